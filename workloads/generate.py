@@ -1,0 +1,118 @@
+"""Seeded synthetic inputs shared by the tests, the bench and the oracle.
+
+This module draws random numbers and lays tensors out; it holds none of the
+method's arithmetic (no summaries, scores, selection or attention).
+
+Recipe (per layer): a ``torch.Generator`` seeded with ``Workload.seed(layer)``
+draws q, then K, then V, each ~N(0, 1) in fp32 and rounded to bf16. Then:
+  * needles: for every listed block n and every token of it, the key of KV
+    head j is bf16(4 * q[first query head of j's group]) (a power-of-two scale,
+    so it is exact);
+  * outlier channels: K[..., j, c] *= scale for c < outlier_channels;
+  * drift: K[t, j, c] += amp * sin(2*pi*t/period + 2*pi*(j*d + c)/(H_kv*d)),
+    added in fp32 before the bf16 rounding.
+
+Device layout (paged cache): K and V pages are [n_pages][H_kv][B][d] bf16; the
+block table [batch][max_blocks] int32 maps a sequence's logical block to its
+page. ``perm=True`` scatters logical blocks over pages in a seeded random
+order so that every path goes through the table.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from .configs import Workload
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _randn_bf16(shape, g, device) -> torch.Tensor:
+    return torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+
+
+def generate_layer(w: Workload, layer: int = 0, device="cpu", max_blocks: int | None = None,
+                   perm: bool = True, seq_lens=None, seed: int | None = None) -> dict:
+    """Inputs of one layer of one decode step.
+
+    Returns dict with q [b][H_q][d] bf16, k_pages / v_pages [n_pages][H_kv][B][d]
+    bf16, block_table [b][max_blocks] int32 and seq_lens [b] int32 (all on
+    ``device``). ``max_blocks`` may exceed the blocks in use (room to append).
+    """
+    b, Hq, Hkv, d, B = w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size
+    N = w.n_blocks
+    MB = max(N, max_blocks or 0)
+    g = _gen(w.seed(layer) if seed is None else seed, device)
+    q32 = _randn_bf16((b, Hq, d), g, device)
+    q = q32.to(torch.bfloat16)
+    # K and V are drawn in the logical blocked layout [b][MB][H_kv][B][d].
+    k32 = _randn_bf16((b, MB, Hkv, B, d), g, device)
+    if w.outlier_channels:
+        k32[..., : w.outlier_channels] *= w.outlier_scale
+    if w.drift_amp:
+        t = torch.arange(MB * B, device=device, dtype=torch.float32).view(MB, 1, B, 1)
+        jc = (torch.arange(Hkv, device=device, dtype=torch.float32).view(1, Hkv, 1, 1) * d
+              + torch.arange(d, device=device, dtype=torch.float32).view(1, 1, 1, d))
+        phase = 2 * math.pi * t / w.drift_period + 2 * math.pi * jc / (Hkv * d)
+        k32 += w.drift_amp * torch.sin(phase).unsqueeze(0)
+        del t, jc, phase
+    kb = k32.to(torch.bfloat16)
+    del k32
+    if w.needles:
+        G = Hq // Hkv
+        needle_key = (4.0 * q32[:, ::G, :]).to(torch.bfloat16)  # [b][H_kv][d]
+        for n in w.needles:
+            kb[:, n] = needle_key[:, :, None, :].expand(b, Hkv, B, d)
+    vb = _randn_bf16((b, MB, Hkv, B, d), g, device).to(torch.bfloat16)
+    n_pages = b * MB
+    if perm:
+        gp = _gen((w.seed(layer) if seed is None else seed) + 7919, "cpu")
+        page_of = torch.randperm(n_pages, generator=gp).to(torch.int32)
+    else:
+        page_of = torch.arange(n_pages, dtype=torch.int32)
+    block_table = page_of.view(b, MB).to(device)
+    k_pages = torch.empty((n_pages, Hkv, B, d), dtype=torch.bfloat16, device=device)
+    v_pages = torch.empty_like(k_pages)
+    idx = page_of.to(device=device, dtype=torch.long)
+    k_pages[idx] = kb.view(n_pages, Hkv, B, d)
+    v_pages[idx] = vb.view(n_pages, Hkv, B, d)
+    del kb, vb
+    if seq_lens is None:
+        seq_lens = torch.full((b,), w.seq_len, dtype=torch.int32)
+    seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32).to(device)
+    return dict(q=q, k_pages=k_pages, v_pages=v_pages, block_table=block_table.contiguous(),
+                seq_lens=seq_lens, max_blocks=MB)
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> numpy uint16 bit patterns (a reinterpretation, no rounding)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def logical_kv(pages: torch.Tensor, block_table: torch.Tensor, b: int, T: int) -> torch.Tensor:
+    """One sequence's cache in token order [T][H_kv][d], gathered from its pages."""
+    B = pages.shape[2]
+    N = (T + B - 1) // B
+    p = block_table[b, :N].long().to(pages.device)
+    blk = pages[p]                                  # [N][H_kv][B][d]
+    return blk.permute(0, 2, 1, 3).reshape(N * B, pages.shape[1], pages.shape[3])[:T]
+
+
+def host_tier_layout(k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
+                     n_blocks: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Offload-tier layout [b][N][2][H_kv][B][d]: K then V of one block contiguous."""
+    b = block_table.shape[0]
+    _, Hkv, B, d = k_pages.shape
+    if out is None:
+        out = torch.empty((b, n_blocks, 2, Hkv, B, d), dtype=torch.bfloat16)
+    for s in range(b):
+        p = block_table[s, :n_blocks].long().to(k_pages.device)
+        out[s, :, 0].copy_(k_pages[p])
+        out[s, :, 1].copy_(v_pages[p])
+    return out
