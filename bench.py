@@ -1,0 +1,486 @@
+"""Benchmark: query-aware block selection + sparse decode attention on GB300.
+
+Default workload: the Qwen3-4B-shaped GQA batch decode (batch 16, 32 q / 8 KV
+heads, head_dim 128, 32768 cached tokens in blocks of 32, keep 12.5 % = 128
+blocks, 36 layers with distinct buffers, about 74 GB of KV on the device).
+
+One step = one decode step through all 36 layers; per layer it runs every
+step of the hot path through the C ABI: the budget (host), the append of the
+new token with the open block's summary update, score + Top-k + spans, and
+the sparse decode attention. The metric is layer-steps per second.
+
+Device timing: CUDA events on the bench stream around exactly --steps steps
+after --warmup steps, with a device sync (and a barrier under torchrun) on
+both sides; the max over ranks is reported. The 36 distinct layers (74 GB)
+exceed the 129 MB L2, so no flush is needed between steps. Each decode and
+score launch is also bracketed by events for the per-kernel roofline.
+
+--impl reference times the fp64 CPU oracle on this machine's host cores on a
+bounded sample (one layer, a few sequences) of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode-attn steps/s per layer; achieved HBM GB/s vs GB300 peak"
+UNIT = "layer-steps/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvsel", choices=["kvsel", "reference"])
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (debug)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks ---
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ GPU workload ---
+
+class Workbench:
+    """All layers of the workload resident on the device, plus per-step inputs."""
+
+    def __init__(self, w, layers, total_steps, device):
+        import torch
+
+        from query_aware_sparse_block_gb300.runtime import SparseDecoder
+        from workloads.generate import generate_layer
+
+        self.w, self.L, self.device = w, layers, device
+        B = w.block_size
+        self.T0 = w.seq_len
+        self.max_blocks = (self.T0 + total_steps + B - 1) // B + 1
+        self.k = w.k_for(w.keep[0])
+        self.dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, B, self.max_blocks,
+                                 k_max=self.k, device=device)
+        self.layers = []
+        for l in range(layers):
+            x = generate_layer(w, l, device=device, max_blocks=self.max_blocks, perm=False)
+            summ, acc = self.dec.new_summaries()
+            self.dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
+            g = torch.Generator(device=device)
+            g.manual_seed(w.seed(l) + 104729)
+            shape = (w.batch, w.n_kvheads, w.head_dim)
+            new_k = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+            new_v = torch.randn(shape, generator=g, device=device).to(torch.bfloat16)
+            out = torch.empty((w.batch, w.n_qheads, w.head_dim), dtype=torch.float32, device=device)
+            lse = torch.empty((w.batch, w.n_qheads), dtype=torch.float32, device=device)
+            self.layers.append(dict(x=x, summ=summ, acc=acc, new_k=new_k, new_v=new_v, out=out,
+                                    lse=lse))
+            torch.cuda.synchronize()
+        # per-step positions: step s appends token T0 + s, then attends over T0 + s + 1 tokens
+        s = torch.arange(total_steps, device=device, dtype=torch.int32).view(-1, 1)
+        self.append_pos = (self.T0 + s).expand(total_steps, w.batch).contiguous()
+        self.seq_lens = self.append_pos + 1
+        self.dec.k_per_seq.fill_(self.k)
+        self.step_i = 0
+        self.kv_src = [None] * layers
+        from query_aware_sparse_block_gb300 import kvsel as K
+        self.K = K
+        for l, d in enumerate(self.layers):
+            self.kv_src[l] = K.kv_paged(d["x"]["k_pages"], d["x"]["v_pages"], d["x"]["block_table"])
+
+    def budget_k(self):
+        """kvsel_budget on the host: keep ratio (12.5 % override, no floor) -> k."""
+        w = self.w
+        N = (self.T0 + self.step_i + w.block_size) // w.block_size
+        r = self.K.kvsel_budget(w.block_size, w.n_kvheads, w.head_dim, 2, 2560, N, 6.7e12, 1.7e15,
+                                keep_override=w.keep[0], gamma=w.gamma)
+        return r
+
+    def step(self, stream, ev_score=None, ev_dec=None, q_list=None, out_list=None, nk_list=None,
+             nv_list=None):
+        """One decode step through all layers (enqueue only)."""
+        i = self.step_i
+        pos = self.append_pos[i]
+        lens = self.seq_lens[i]
+        self.budget_k()
+        for l, d in enumerate(self.layers):
+            x = d["x"]
+            q = x["q"] if q_list is None else q_list[l]
+            nk = d["new_k"] if nk_list is None else nk_list[l]
+            nv = d["new_v"] if nv_list is None else nv_list[l]
+            out = d["out"] if out_list is None else out_list[l]
+            self.dec.append(x["k_pages"], x["v_pages"], x["block_table"], pos, d["summ"], d["acc"],
+                            new_k=nk, new_v=nv, stream=stream)
+            if ev_score is not None:
+                ev_score[0][l].record(stream)
+            self.dec.select(q, d["summ"], lens, gamma=self.w.gamma, stream=stream)
+            if ev_score is not None:
+                ev_score[1][l].record(stream)
+            if ev_dec is not None:
+                ev_dec[0][l].record(stream)
+            self.dec.attend(q, self.kv_src[l], lens, out=out, lse=d["lse"], stream=stream)
+            if ev_dec is not None:
+                ev_dec[1][l].record(stream)
+        self.step_i += 1
+
+    def decode_bytes(self):
+        w = self.w
+        sel = self.k * w.n_kvheads * 2 * w.block_size * w.head_dim * 2 * w.batch
+        q = w.batch * w.n_qheads * w.head_dim * 2
+        out = w.batch * w.n_qheads * (w.head_dim + 1) * 4
+        return sel + q + out
+
+    def score_bytes(self, N):
+        w = self.w
+        summ = w.batch * N * w.n_kvheads * w.head_dim * 2
+        q = w.batch * w.n_qheads * w.head_dim * 2
+        scores = w.batch * N * 4
+        sel = w.batch * self.k * 4 * 3
+        return summ + q + scores + sel
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    from workloads import C3
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = C3
+    layers = args.layers or w.layers
+    n_e2e = 0 if args.no_e2e else max(3, args.steps // 2)
+    total_steps = args.warmup + args.steps + 2 + n_e2e + 2
+    wb = Workbench(w, layers, total_steps, device)
+    K = wb.K
+    stream = torch.cuda.Stream(device=device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            wb.step(stream)
+        stream.synchronize()
+        err = K.kvsel_get_error(stream)
+        if err:
+            raise RuntimeError(f"device error {err} during warm-up")
+        ev_s = [[torch.cuda.Event(enable_timing=True) for _ in range(layers * args.steps)] for _ in range(2)]
+        ev_d = [[torch.cuda.Event(enable_timing=True) for _ in range(layers * args.steps)] for _ in range(2)]
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        clocks = ClockSampler(local)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clocks.start()
+        launches0 = K.kvsel_launch_count()
+        t0.record(stream)
+        for s in range(args.steps):
+            sl = slice(s * layers, (s + 1) * layers)
+            wb.step(stream, ev_score=(ev_s[0][sl], ev_s[1][sl]), ev_dec=(ev_d[0][sl], ev_d[1][sl]))
+        t1.record(stream)
+        stream.synchronize()
+        launches = K.kvsel_launch_count() - launches0
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        clk = clocks.stop()
+        elapsed_ms = t0.elapsed_time(t1)
+        err = K.kvsel_get_error(stream)
+        if err:
+            raise RuntimeError(f"device error {err} in the timed region")
+        if world > 1:
+            t = torch.tensor([elapsed_ms], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            elapsed_ms = float(t.item())
+        dec_ms = [a.elapsed_time(b) for a, b in zip(ev_d[0], ev_d[1])]
+        sc_ms = [a.elapsed_time(b) for a, b in zip(ev_s[0], ev_s[1])]
+
+        # ---- e2e: pinned host inputs in, results out, through the public API ----
+        e2e = None
+        if n_e2e:
+            q_host = torch.stack([d["x"]["q"] for d in wb.layers]).cpu().pin_memory()
+            kv_host = torch.stack([torch.stack([d["new_k"], d["new_v"]]) for d in wb.layers]).cpu().pin_memory()
+            q_dev = torch.empty_like(q_host, device=device)
+            kv_dev = torch.empty_like(kv_host, device=device)
+            out_dev = torch.empty((layers, w.batch, w.n_qheads, w.head_dim), dtype=torch.float32, device=device)
+            out_host = torch.empty(out_dev.shape, dtype=torch.float32).pin_memory()
+            nks = [kv_dev[l, 0] for l in range(layers)]
+            nvs = [kv_dev[l, 1] for l in range(layers)]
+            qs = [q_dev[l] for l in range(layers)]
+            outs = [out_dev[l] for l in range(layers)]
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(n_e2e):
+                q_dev.copy_(q_host, non_blocking=True)
+                kv_dev.copy_(kv_host, non_blocking=True)
+                wb.step(stream, q_list=qs, out_list=outs, nk_list=nks, nv_list=nvs)
+                out_host.copy_(out_dev, non_blocking=True)
+            e1.record(stream)
+            stream.synchronize()
+            e2e_ms = e0.elapsed_time(e1) / n_e2e
+            e2e = {"value": layers / (e2e_ms / 1e3), "unit": UNIT,
+                   "h2d_bytes_per_step": q_host.numel() * 2 + kv_host.numel() * 2,
+                   "d2h_bytes_per_step": out_host.numel() * 4,
+                   "ms_per_step": e2e_ms, "steps": n_e2e}
+
+    ms_per_step = elapsed_ms / args.steps
+    value = world * layers * args.steps / (elapsed_ms / 1e3)
+    peak, peak_kind = peaks()
+    N = (wb.T0 + args.warmup + w.block_size) // w.block_size   # blocks at the first timed step
+    dec_bytes = wb.decode_bytes()
+    dec_avg_ms = statistics.mean(dec_ms)
+    sc_avg_ms = statistics.mean(sc_ms)
+    dec_gbs = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+    sc_bytes = wb.score_bytes(N)
+    sc_gbs = sc_bytes / (sc_avg_ms / 1e3) / 1e9
+    traffic = None
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            traffic = json.load(f).get("sparse_decode_c3_bytes_per_launch")
+    except Exception:
+        pass
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "n_qheads": w.n_qheads,
+                   "n_kvheads": w.n_kvheads, "head_dim": w.head_dim, "seq_len": w.seq_len,
+                   "block_size": w.block_size, "keep": w.keep[0], "k": wb.k, "layers": layers,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (distinct buffers per layer, no flush)"},
+        "roofline": {"kernel": "sparse_decode", "bound": "hbm", "achieved": dec_gbs, "peak": peak,
+                     "unit": "GB/s", "frac": dec_gbs / peak, "peak_kind": peak_kind,
+                     "traffic": traffic, "bytes_per_launch": dec_bytes,
+                     "avg_launch_us": dec_avg_ms * 1e3},
+        "kernels": {
+            "score_topk": {"bytes_per_launch": sc_bytes, "avg_launch_us": sc_avg_ms * 1e3,
+                           "achieved_gbs": sc_gbs, "frac": sc_gbs / peak},
+            "sparse_decode": {"bytes_per_launch": dec_bytes, "avg_launch_us": dec_avg_ms * 1e3,
+                              "achieved_gbs": dec_gbs, "frac": dec_gbs / peak},
+        },
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_subprocess(args.ref_seqs, reps=3)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------ oracle (reference) ---
+
+def oracle_sample_inputs(n_seqs: int):
+    """One layer of the workload on the CPU, restricted to the first sequences."""
+    from workloads import C3
+    from workloads.generate import bits, generate_layer, logical_kv
+
+    w = C3.scaled(batch=n_seqs)
+    x = generate_layer(w, 0, device="cpu", perm=False)
+    seqs = []
+    for b in range(n_seqs):
+        seqs.append(dict(q=bits(x["q"][b]), k=bits(logical_kv(x["k_pages"], x["block_table"], b, w.seq_len)),
+                         v=bits(logical_kv(x["v_pages"], x["block_table"], b, w.seq_len))))
+    return w, seqs
+
+
+def oracle_step(w, seqs, k, scale, state):
+    """The decode step of one layer on the sampled sequences, in the oracle:
+    append of the last token into the open block, score, Top-k, spans, gamma
+    rule and attention over the selected blocks."""
+    import oracle as o
+
+    T = w.seq_len
+    for s, st in zip(seqs, state):
+        _, sb_open = o.append_token(st["acc"], s["k"][T - 1], T - 1, w.block_size)
+        summ = st["bits"].copy()
+        summ[(T - 1) // w.block_size] = sb_open
+        scores = o.block_scores(s["q"], summ)
+        sel = o.topk_blocks(scores, k)
+        starts, _ = o.merge_spans(sel)
+        dense = o.dense_fallback(len(starts), len(sel), len(scores), w.gamma, 0.0)
+        blocks = np.arange(len(scores)) if dense else sel
+        o.attend(s["q"], s["k"], s["v"], o.tokens_of_blocks(blocks, T, w.block_size), scale)
+
+
+def oracle_state(w, seqs):
+    """Summaries of the first T-1 tokens and the open block's accumulator."""
+    import oracle as o
+
+    state = []
+    for s in seqs:
+        bits_, _, acc = o.block_summaries(s["k"], w.seq_len - 1, w.block_size)
+        full = np.zeros((w.n_blocks,) + bits_.shape[1:], dtype=np.uint16)
+        full[: bits_.shape[0]] = bits_
+        state.append(dict(bits=full, acc=acc))
+    return state
+
+
+def _oracle_worker(n_seqs, reps, out_path):
+    w, seqs = oracle_sample_inputs(n_seqs)
+    state = oracle_state(w, seqs)
+    k = w.k_for(w.keep[0])
+    scale = 1.0 / math.sqrt(w.head_dim)
+    times = []
+    for _ in range(reps):
+        t = time.perf_counter()
+        oracle_step(w, seqs, k, scale, state)
+        times.append(time.perf_counter() - t)
+    with open(out_path, "w") as f:
+        json.dump({"times": times, "n_seqs": n_seqs, "batch": 16}, f)
+
+
+def cpu_baseline_subprocess(n_seqs: int, reps: int):
+    """Times the oracle in a fresh process with the BLAS thread count pinned."""
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    with tempfile.TemporaryDirectory() as td:
+        out = os.path.join(td, "o.json")
+        code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench; "
+                f"bench._oracle_worker({n_seqs}, {reps}, {out!r})")
+        subprocess.run([sys.executable, "-c", code], env=env, check=True, timeout=900)
+        with open(out) as f:
+            r = json.load(f)
+    t = statistics.median(r["times"])
+    layer_step_s = t * r["batch"] / r["n_seqs"]
+    return {"value": 1.0 / layer_step_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"one layer, {n_seqs} of 16 sequences (append, score, Top-k, spans, "
+                      f"attention over 128 blocks); median of {reps}; scaled to a 16-sequence layer-step",
+            "seconds_per_sample": t}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads import C3
+
+    cores = len(os.sched_getaffinity(0))
+    w, seqs = oracle_sample_inputs(args.ref_seqs)
+    state = oracle_state(w, seqs)
+    k = w.k_for(w.keep[0])
+    scale = 1.0 / math.sqrt(w.head_dim)
+    for _ in range(args.warmup):
+        oracle_step(w, seqs, k, scale, state)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, seqs, k, scale, state)
+    el = time.perf_counter() - t
+    per_layer_step = el / args.steps * (C3.batch / args.ref_seqs)
+    value = 1.0 / per_layer_step
+    sample = (f"each step: one layer, {args.ref_seqs} of {C3.batch} sequences of {C3.name} "
+              f"(append, score, Top-k, spans, attention); scaled to a {C3.batch}-sequence layer-step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer_step * 1e3 * C3.layers,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": C3.name, "batch": C3.batch, "seq_len": C3.seq_len,
+                       "layers": C3.layers, "k": k, "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

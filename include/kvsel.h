@@ -1,0 +1,296 @@
+/*
+ * kvsel.h -- C ABI of the query-aware sparse KV-block selection and sparse
+ * decode-attention library (libkvsel.so), written for NVIDIA GB300 (sm_103a).
+ *
+ * The method is SparPR's decode-step loop ("SparPR KV cache recovery on a
+ * consumer GPU", section "Three decisions rather than one compression
+ * ratio"): every cached KV block is summarised by its mean key per KV head;
+ * a query scores each block by the sum over heads of query.summary inner
+ * products; Top-k picks the blocks; adjacent picks merge into spans; a cost
+ * model (copy vs recompute) with a Minimum Keep Floor sets the keep ratio and
+ * a Dense Fallback Threshold gamma switches back to full attention. Attention
+ * then runs over the selected blocks only, with split partial results merged
+ * by log-sum-exp (the flash-style merge of the DKV abstract).
+ *
+ * Conventions shared by every entry point
+ *  - Return value: KVSEL_OK (0) or a KVSEL_ERR_* code. No entry point aborts,
+ *    traps the device or allocates device memory. Host-side argument checks
+ *    return KVSEL_ERR_INVALID_ARG / KVSEL_ERR_UNSUPPORTED before anything is
+ *    enqueued. Launch failures return KVSEL_ERR_CUDA.
+ *  - Data-dependent faults found by a kernel (an out-of-range block-table
+ *    entry, page, selection index or count) are not fatal: the kernel skips
+ *    the offending access, latches the first error code into a per-device
+ *    error word and carries on. kvsel_get_error() reads and clears it.
+ *  - Device entry points are asynchronous on the caller's stream; the caller
+ *    owns every buffer. Scratch comes from a caller workspace whose size
+ *    kvsel_workspace_size() returns; a workspace must be zero-filled before
+ *    its first use and each call leaves it zero-filled again.
+ *  - bf16 tensors are passed as kvsel_bf16 (the 16-bit pattern). Device
+ *    pointers must be 16-byte aligned.
+ *  - Supported shapes: head_dim in {64, 128}; block_size in {16, 32, 64};
+ *    n_qheads a multiple of n_kvheads with n_qheads / n_kvheads <= 16;
+ *    batch <= 4096; max_blocks <= 16384; n_kvheads * head_dim / 8 a power
+ *    of two times a divisor of 32 whose quotient is at most 16.
+ *
+ * Layouts (row-major, innermost last)
+ *  q            [batch][n_qheads][head_dim]                    bf16
+ *  K / V pages  [n_pages][n_kvheads][block_size][head_dim]     bf16
+ *  block_table  [batch][max_blocks]                            int32 (page id)
+ *  seq_lens     [batch]                                        int32 (T_b)
+ *  summaries    [batch][max_blocks][n_kvheads][head_dim]       bf16
+ *  open_acc     [batch][n_kvheads][head_dim]                   fp64
+ *  sel_idx      [batch][k_max]  ascending block indices        int32
+ *  spans        span_start / span_len [batch][k_max]           int32
+ *  host tier    [batch][host_blocks][2][n_kvheads][block_size][head_dim] bf16
+ *               (K then V of one block contiguous, spans contiguous)
+ *  staging      [batch][staging_slots][2][n_kvheads][block_size][head_dim] bf16
+ *  out          [batch][n_qheads][head_dim] fp32; lse [batch][n_qheads] fp32
+ * A sequence b holds T_b = seq_lens[b] tokens in N_b = ceil(T_b / block_size)
+ * blocks; token t lives in page block_table[b][t / block_size], row
+ * t % block_size.
+ */
+#ifndef KVSEL_H_
+#define KVSEL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVSEL_VERSION_STRING "kvsel 0.1.0 (sm_103a)"
+
+#if defined(__GNUC__)
+#define KVSEL_API __attribute__((visibility("default")))
+#else
+#define KVSEL_API
+#endif
+
+typedef uint16_t kvsel_bf16;               /* bf16 bit pattern */
+typedef struct CUstream_st* kvsel_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum kvsel_status {
+  KVSEL_OK = 0,
+  KVSEL_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or shape */
+  KVSEL_ERR_CUDA = 2,         /* a CUDA runtime call or launch failed */
+  KVSEL_ERR_BOUNDS = 3,       /* device-detected out-of-range index or count */
+  KVSEL_ERR_TIMEOUT = 4,      /* a bounded device wait ran out */
+  KVSEL_ERR_UNSUPPORTED = 5,  /* shape outside the compiled variants */
+  KVSEL_ERR_WORKSPACE = 6     /* workspace missing or smaller than required */
+};
+
+/* Shape of one layer's decode step. */
+typedef struct kvsel_problem {
+  int32_t batch;       /* sequences in the batch */
+  int32_t n_qheads;    /* query heads H_q */
+  int32_t n_kvheads;   /* KV heads H_kv (GQA group G = H_q / H_kv) */
+  int32_t head_dim;    /* d */
+  int32_t block_size;  /* B, tokens per block (= per page) */
+  int32_t max_blocks;  /* row stride of block_table and summaries (blocks per sequence capacity) */
+  int32_t k_max;       /* row stride of sel_idx / span arrays (selection capacity) */
+} kvsel_problem;
+
+enum kvsel_summary_mode {
+  KVSEL_SUMMARY_FULL = 0,   /* rebuild every block summary of every sequence */
+  KVSEL_SUMMARY_APPEND = 1  /* fold one appended token per sequence into its open block */
+};
+
+/*
+ * kvsel_build_summaries -- block summaries ("SparPR KV cache recovery on a
+ * consumer GPU", paragraph "Query-Aware key-block selection": each block gets
+ * a compact precomputed summary, the mean key; kept resident on the GPU).
+ *
+ * summaries[b][n][j][:] = bf16_rne( (sum over the block's tokens t < T_b of
+ * K[t][j][:]) / count ), the sum taken in fp64 in token order from +0.0, the
+ * division in fp64 and one round-to-nearest-even to bf16.
+ *
+ * FULL:   for every b and every block n < N_b. open_acc[b] receives the fp64
+ *         sum of block N_b - 1 (the open block). new_k/new_v/append_pos unused.
+ * APPEND: for every b with t = append_pos[b] >= 0 (others are skipped): if
+ *         new_k != NULL, new_k[b][j][:] is first written to K row t (and new_v
+ *         to V row t when new_v != NULL); then open_acc[b] becomes K_t when
+ *         t % B == 0 (a new block) or open_acc[b] + K_t otherwise, and the
+ *         summary of block t / B is rewritten from it over t % B + 1 tokens.
+ *         The caller sets seq_lens[b] = t + 1 for the steps that follow.
+ *
+ * k_pages, v_pages: paged cache (v_pages only written by APPEND with new_v).
+ * block_table, seq_lens: device int32. append_pos: device [batch] int32.
+ * new_k, new_v: device [batch][n_kvheads][head_dim] bf16, nullable.
+ * summaries: device output. open_acc: device [batch][n_kvheads][head_dim] fp64.
+ * Errors: INVALID_ARG (null required pointer, bad shape), UNSUPPORTED, CUDA;
+ * device BOUNDS when a block-table entry is negative or >= n_pages or
+ * T_b > max_blocks * B (the access is skipped).
+ */
+KVSEL_API int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16* k_pages,
+                          kvsel_bf16* v_pages, int64_t n_pages, const int32_t* block_table,
+                          const int32_t* seq_lens, const int32_t* append_pos,
+                          const kvsel_bf16* new_k, const kvsel_bf16* new_v,
+                          kvsel_bf16* summaries, double* open_acc, kvsel_stream_t stream);
+
+/*
+ * kvsel_score_topk -- query-aware block score, Top-k and span merge in one
+ * launch ("SparPR KV cache recovery on a consumer GPU", paragraphs
+ * "Query-Aware key-block selection" and "On-demand local recomputation with
+ * cost-aware fallback").
+ *
+ * score[b][n] = sum over query heads h of <q[b][h], summaries[b][n][kv(h)]>,
+ * kv(h) = h / G, accumulated in fp32 (q is first folded over each GQA group).
+ * k_b = min(k_per_seq[b], N_b, k_max) blocks with the largest scores are
+ * selected, ties to the lower block index; sel_idx[b][0..k_b) holds them in
+ * ascending order and n_sel[b] = k_b. Runs of consecutive indices become
+ * spans: span_start / span_len [b][0..n_spans[b]).
+ * Dense fallback (gamma): dense_flag[b] = (n_spans * tau_rel + k_b >=
+ * gamma * (tau_rel + N_b)), evaluated in fp64; tau_rel is the per-span
+ * overhead in units of one block's recovery cost (0 gives k_b >= gamma*N_b).
+ *
+ * q: device [batch][n_qheads][head_dim] bf16. summaries: device.
+ * k_per_seq: device [batch] int32 (k_per_seq[b] > k_max latches BOUNDS and
+ * is clamped). scores_out: device [batch][max_blocks] fp32, nullable.
+ * dense_flag: device [batch] uint8, nullable. ws: workspace of
+ * kvsel_workspace_size(p, KVSEL_WS_SCORE_TOPK) bytes.
+ */
+KVSEL_API int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_bf16* summaries,
+                     const int32_t* seq_lens, const int32_t* k_per_seq, float gamma,
+                     float tau_rel, int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                     int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                     float* scores_out, void* ws, size_t ws_bytes, kvsel_stream_t stream);
+
+/*
+ * kvsel_merge_spans -- span merge of an existing ascending selection ("SparPR
+ * KV cache recovery on a consumer GPU", paragraph "On-demand local
+ * recomputation with cost-aware fallback": adjacent blocks merge into
+ * continuous spans). Indices that differ by exactly one join a span.
+ * sel_idx [batch][k_max] with n_sel[b] entries (device); outputs as in
+ * kvsel_score_topk. A selection that is not strictly ascending latches BOUNDS.
+ */
+KVSEL_API int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, const int32_t* n_sel,
+                      int32_t* span_start, int32_t* span_len, int32_t* n_spans,
+                      kvsel_stream_t stream);
+
+enum kvsel_kv_kind {
+  KVSEL_KV_PAGED = 0,  /* K/V pages in device memory + block table */
+  KVSEL_KV_STAGED = 1, /* selected blocks already in a device staging buffer */
+  KVSEL_KV_HOST = 2    /* full K/V in pinned host memory: fetch the spans, then attend */
+};
+
+/* Where the K/V of the attended blocks come from. */
+typedef struct kvsel_kv_src {
+  int32_t kind;                   /* enum kvsel_kv_kind */
+  int32_t staging_slots;          /* STAGED/HOST: block slots per sequence in staging */
+  const kvsel_bf16* k_pages;      /* PAGED */
+  const kvsel_bf16* v_pages;      /* PAGED */
+  const int32_t* block_table;     /* PAGED */
+  int64_t n_pages;                /* PAGED: pages in k_pages and v_pages */
+  kvsel_bf16* staging;            /* STAGED/HOST: device staging buffer */
+  const kvsel_bf16* host_kv;      /* HOST: pinned host tier (device-mapped) */
+  int32_t host_blocks;            /* HOST: block stride of the host tier per sequence */
+  int32_t fetch_ctas;             /* HOST: CTAs of the gather kernel (0 = one per SM) */
+} kvsel_kv_src;
+
+/*
+ * kvsel_sparse_decode -- attention over the selected blocks only ("SparPR KV
+ * cache recovery on a consumer GPU", paragraph "On-demand local
+ * recomputation with cost-aware fallback"; split partial results merged by
+ * the flash-style log-sum-exp reduction of the DKV abstract).
+ *
+ * For every b and query head h: out[b][h] = sum_t softmax_t(scale * q.K_t) V_t
+ * over the tokens t < T_b of the blocks sel_idx[b][0..n_sel[b]) -- or of all
+ * N_b blocks when dense_flag != NULL and dense_flag[b] != 0 -- using KV head
+ * h / G. lse[b][h] = ln sum_t exp(scale * q.K_t). A sequence with no attended
+ * token gets out = 0 and lse = -inf. Math in fp32 (bf16 tensor-core products,
+ * fp32 accumulation).
+ *
+ * kv: see kvsel_kv_src. STAGED: the o-th attended block of b is staging slot
+ * o (block n when dense). HOST: the selected spans (or all blocks when dense)
+ * are first gathered from host_kv into staging on `stream` (see
+ * kvsel_fetch_spans), then treated as STAGED.
+ * out: device fp32 output; out_bf16: optional bf16 copy; lse: device fp32.
+ * ws: kvsel_workspace_size(p, KVSEL_WS_SPARSE_DECODE) bytes.
+ */
+KVSEL_API int kvsel_sparse_decode(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_kv_src* kv,
+                        const int32_t* seq_lens, const int32_t* sel_idx, const int32_t* n_sel,
+                        const int32_t* span_start, const int32_t* span_len,
+                        const int32_t* n_spans, const uint8_t* dense_flag, float softmax_scale,
+                        float* out, kvsel_bf16* out_bf16, float* lse, void* ws,
+                        size_t ws_bytes, kvsel_stream_t stream);
+
+/*
+ * kvsel_fetch_spans -- the offload tier's recovery copy: full K/V stays in
+ * pinned host memory and only the selected spans cross the host link ("KV
+ * cache offloading", sections "Fetching a sparse subset per step" and "NOSA":
+ * a kernel that reads host memory directly through unified virtual
+ * addressing). A gather kernel of kv->fetch_ctas CTAs reads each span's
+ * contiguous blocks from kv->host_kv and writes them to consecutive staging
+ * slots; with dense_flag[b] set it copies all N_b blocks. No host round trip.
+ * Requires kind == KVSEL_KV_HOST. Returns INVALID_ARG when host_kv is not
+ * device-accessible.
+ */
+KVSEL_API int kvsel_fetch_spans(const kvsel_problem* p, const kvsel_kv_src* kv, const int32_t* seq_lens,
+                      const int32_t* span_start, const int32_t* span_len,
+                      const int32_t* n_spans, const uint8_t* dense_flag,
+                      kvsel_stream_t stream);
+
+/* Budget inputs ("SparPR KV cache recovery on a consumer GPU", paragraph
+ * "Dynamic budget control"). */
+typedef struct kvsel_budget_in {
+  int32_t block_size, kv_heads, head_dim, elem_bytes; /* one block of one layer */
+  int64_t hidden;                /* model hidden size */
+  int64_t n_blocks;              /* candidate blocks N */
+  double h2d_bytes_per_s;        /* bandwidth the blocks are recovered over */
+  double recompute_flop_per_s;   /* throughput of the recompute path */
+  double kappa;                  /* flops per multiply-add of the recompute (2) */
+  double keep_floor;             /* Minimum Keep Floor */
+  double gamma;                  /* Dense Fallback Threshold */
+  double tau_s;                  /* per-span recovery overhead, seconds */
+  double keep_override;          /* >= 0: use this ratio instead of the model's */
+} kvsel_budget_in;
+
+typedef struct kvsel_budget_out {
+  double c_copy_s;   /* 2 * S_blk / BW, S_blk = B * H_kv * d * elem_bytes */
+  double c_rec_s;    /* kappa * B * hidden^2 / F */
+  double r_model;    /* c_rec / c_copy */
+  double r;          /* min(1, max(keep_floor, keep_override >= 0 ? keep_override : r_model)) */
+  int64_t k;         /* clamp(floor(r * N + 1/2), 1, N); 0 when N = 0 */
+  double tau_rel;    /* tau_s / c_copy */
+  int32_t dense;     /* 1 if even a single-span sparse recovery is not clearly cheaper */
+} kvsel_budget_out;
+
+/*
+ * kvsel_budget -- host-only, pure. The per-block copy cost is data volume over
+ * host-to-device bandwidth with a factor 2 for K and V; the recompute cost
+ * grows with block length and the square of the hidden size; their ratio
+ * maps to the keep ratio, bounded below by the Minimum Keep Floor ("SparPR KV
+ * cache recovery on a consumer GPU", paragraph "Dynamic budget control").
+ * The dense decision uses the gamma rule of kvsel_score_topk with one span.
+ * Errors: INVALID_ARG for null pointers, non-positive sizes or bandwidths.
+ */
+KVSEL_API int kvsel_budget(const kvsel_budget_in* in, kvsel_budget_out* out);
+
+enum kvsel_ws_kind { KVSEL_WS_SCORE_TOPK = 0, KVSEL_WS_SPARSE_DECODE = 1 };
+
+/* Workspace bytes an entry point needs for problem p (0 on bad input). */
+KVSEL_API size_t kvsel_workspace_size(const kvsel_problem* p, int which);
+
+/* KV bytes per cached token: 2 * layers * kv_heads * head_dim * elem_bytes
+ * ("KV cache offloading", section "Why the cache leaves the GPU"). -1 on
+ * negative input. */
+KVSEL_API int64_t kvsel_kv_bytes_per_token(int32_t layers, int32_t kv_heads, int32_t head_dim,
+                                 int32_t elem_bytes);
+
+/* Reads and clears the current device's latched error word after draining
+ * `stream` (a synchronising call). Returns KVSEL_OK or the first device error. */
+KVSEL_API int kvsel_get_error(kvsel_stream_t stream);
+
+/* Kernel launches made by this library since load (host-side counter). */
+KVSEL_API uint64_t kvsel_launch_count(void);
+
+/* Human-readable text of the last host-side error in this thread. */
+KVSEL_API const char* kvsel_last_error(void);
+
+KVSEL_API const char* kvsel_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVSEL_H_ */

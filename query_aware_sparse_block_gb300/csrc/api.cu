@@ -1,0 +1,354 @@
+// C ABI of libkvsel: argument checks, workspace sizing, the host-side budget
+// model and the per-device error word. Kernels live in summaries.cu,
+// score_topk.cu, sparse_decode.cu and offload.cu.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "kvsel_common.cuh"
+#include "kvsel_internal.h"
+
+namespace kvsel {
+
+namespace {
+__device__ int g_error_word;   // latched first device error (0 = none)
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_msg[512] = "";
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+}  // namespace
+
+void set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+}
+
+int* device_error_word() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<int*>(p);
+  }
+  return g_err_ptr[d];
+}
+
+int sm_count() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[d]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = n > 0 ? n : 1;
+  }
+  return g_sms[d];
+}
+
+void count_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }
+
+}  // namespace kvsel
+
+using namespace kvsel;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int fail(int code, const char* what) {
+  set_last_error("%s", what);
+  return code;
+}
+
+int check_problem(const kvsel_problem* p) {
+  if (!p) return fail(KVSEL_ERR_INVALID_ARG, "problem is NULL");
+  if (p->batch < 0 || p->batch > 4096) return fail(KVSEL_ERR_INVALID_ARG, "batch must be in [0, 4096]");
+  if (p->n_qheads <= 0 || p->n_kvheads <= 0 || p->n_qheads % p->n_kvheads)
+    return fail(KVSEL_ERR_INVALID_ARG, "n_qheads must be a positive multiple of n_kvheads");
+  if (p->n_qheads / p->n_kvheads > 16)
+    return fail(KVSEL_ERR_UNSUPPORTED, "GQA group larger than 16 query heads");
+  if (p->head_dim != 64 && p->head_dim != 128)
+    return fail(KVSEL_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (p->block_size != 16 && p->block_size != 32 && p->block_size != 64)
+    return fail(KVSEL_ERR_UNSUPPORTED, "block_size must be 16, 32 or 64");
+  if (p->max_blocks <= 0 || p->max_blocks > 16384)
+    return fail(KVSEL_ERR_INVALID_ARG, "max_blocks must be in [1, 16384]");
+  if (p->k_max <= 0 || p->k_max > p->max_blocks)
+    return fail(KVSEL_ERR_INVALID_ARG, "k_max must be in [1, max_blocks]");
+  const int nv = p->n_kvheads * p->head_dim / 8;
+  int lpb = 32;
+  while (nv % lpb) lpb >>= 1;
+  const int vpl = nv / lpb;
+  if (vpl != 1 && vpl != 2 && vpl != 4 && vpl != 8 && vpl != 16)
+    return fail(KVSEL_ERR_UNSUPPORTED, "n_kvheads * head_dim not supported by the scoring kernel");
+  return KVSEL_OK;
+}
+
+int cuda_status(cudaError_t e, const char* where) {
+  if (e == cudaSuccess) return KVSEL_OK;
+  set_last_error("%s: %s", where, cudaGetErrorString(e));
+  return KVSEL_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvsel_version(void) { return KVSEL_VERSION_STRING; }
+
+const char* kvsel_last_error(void) { return g_msg; }
+
+uint64_t kvsel_launch_count(void) { return g_launches.load(); }
+
+int64_t kvsel_kv_bytes_per_token(int32_t layers, int32_t kv_heads, int32_t head_dim,
+                                 int32_t elem_bytes) {
+  if (layers < 0 || kv_heads < 0 || head_dim < 0 || elem_bytes < 0) return -1;
+  return int64_t(2) * layers * kv_heads * head_dim * elem_bytes;
+}
+
+size_t kvsel_workspace_size(const kvsel_problem* p, int which) {
+  if (check_problem(p) != KVSEL_OK) return 0;
+  if (which == KVSEL_WS_SCORE_TOPK) return score_topk_ws_bytes(*p);
+  if (which == KVSEL_WS_SPARSE_DECODE) return sparse_decode_ws_bytes(*p);
+  return 0;
+}
+
+int kvsel_budget(const kvsel_budget_in* in, kvsel_budget_out* out) {
+  if (!in || !out) return fail(KVSEL_ERR_INVALID_ARG, "budget: NULL argument");
+  if (in->block_size <= 0 || in->kv_heads <= 0 || in->head_dim <= 0 || in->elem_bytes <= 0 ||
+      in->hidden <= 0 || in->n_blocks < 0 || !(in->h2d_bytes_per_s > 0) ||
+      !(in->recompute_flop_per_s > 0) || !(in->kappa > 0))
+    return fail(KVSEL_ERR_INVALID_ARG, "budget: sizes and rates must be positive");
+  const double s_blk = double(in->block_size) * in->kv_heads * in->head_dim * in->elem_bytes;
+  const double c_copy = 2.0 * s_blk / in->h2d_bytes_per_s;
+  const double c_rec = in->kappa * double(in->block_size) * double(in->hidden) *
+                       double(in->hidden) / in->recompute_flop_per_s;
+  const double r_model = c_rec / c_copy;
+  const double r_src = in->keep_override >= 0.0 ? in->keep_override : r_model;
+  const double r = std::fmin(1.0, std::fmax(in->keep_floor, r_src));
+  int64_t k = 0;
+  const int64_t N = in->n_blocks;
+  if (N > 0) {
+    k = int64_t(std::floor(r * double(N) + 0.5));
+    k = k < 1 ? 1 : (k > N ? N : k);
+  }
+  const double tau_rel = in->tau_s / c_copy;
+  int dense = 0;
+  if (N > 0) {
+    const double lhs = 1.0 * tau_rel + double(k);
+    const double rhs = in->gamma * (tau_rel + double(N));
+    dense = lhs >= rhs ? 1 : 0;
+  }
+  out->c_copy_s = c_copy;
+  out->c_rec_s = c_rec;
+  out->r_model = r_model;
+  out->r = r;
+  out->k = k;
+  out->tau_rel = tau_rel;
+  out->dense = dense;
+  return KVSEL_OK;
+}
+
+int kvsel_get_error(kvsel_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int r = cuda_status(cudaStreamSynchronize(s), "kvsel_get_error: stream sync");
+  if (r) return r;
+  int* ew = device_error_word();
+  if (!ew) return fail(KVSEL_ERR_CUDA, "kvsel_get_error: no error word on this device");
+  int h = 0;
+  r = cuda_status(cudaMemcpy(&h, ew, sizeof(int), cudaMemcpyDeviceToHost), "kvsel_get_error: read");
+  if (r) return r;
+  r = cuda_status(cudaMemset(ew, 0, sizeof(int)), "kvsel_get_error: clear");
+  if (r) return r;
+  return h;
+}
+
+int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16* k_pages,
+                          kvsel_bf16* v_pages, int64_t n_pages, const int32_t* block_table,
+                          const int32_t* seq_lens, const int32_t* append_pos,
+                          const kvsel_bf16* new_k, const kvsel_bf16* new_v,
+                          kvsel_bf16* summaries, double* open_acc, kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  if (mode != KVSEL_SUMMARY_FULL && mode != KVSEL_SUMMARY_APPEND)
+    return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: mode must be FULL or APPEND");
+  if (p->batch == 0) return KVSEL_OK;
+  if (!k_pages || !block_table || !summaries || !open_acc || n_pages <= 0)
+    return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: NULL pointer or no pages");
+  if (!aligned16(k_pages) || !aligned16(summaries) || !aligned16(open_acc) ||
+      !aligned4(block_table) || (v_pages && !aligned16(v_pages)))
+    return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: misaligned pointer");
+  if (mode == KVSEL_SUMMARY_FULL && !seq_lens)
+    return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: FULL needs seq_lens");
+  if (mode == KVSEL_SUMMARY_APPEND) {
+    if (!append_pos) return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: APPEND needs append_pos");
+    if ((new_k && !aligned16(new_k)) || (new_v && !aligned16(new_v)))
+      return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: misaligned new_k/new_v");
+    if (new_v && (!new_k || !v_pages))
+      return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: new_v needs new_k and v_pages");
+  }
+  int* ew = device_error_word();
+  if (!ew) return fail(KVSEL_ERR_CUDA, "build_summaries: no CUDA device");
+  return cuda_status(launch_build_summaries(*p, mode, k_pages, v_pages, n_pages, block_table,
+                                            seq_lens, append_pos, new_k, new_v, summaries,
+                                            open_acc, ew, reinterpret_cast<cudaStream_t>(stream)),
+                     "build_summaries launch");
+}
+
+int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_bf16* summaries,
+                     const int32_t* seq_lens, const int32_t* k_per_seq, float gamma,
+                     float tau_rel, int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                     int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                     float* scores_out, void* ws, size_t ws_bytes, kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  if (p->batch == 0) return KVSEL_OK;
+  if (!q || !summaries || !seq_lens || !k_per_seq || !sel_idx || !n_sel || !span_start ||
+      !span_len || !n_spans)
+    return fail(KVSEL_ERR_INVALID_ARG, "score_topk: NULL pointer");
+  if (!aligned16(q) || !aligned16(summaries) || !aligned4(seq_lens) || !aligned4(k_per_seq) ||
+      !aligned4(sel_idx) || !aligned4(n_sel) || !aligned4(span_start) || !aligned4(span_len) ||
+      !aligned4(n_spans) || (scores_out && !aligned4(scores_out)))
+    return fail(KVSEL_ERR_INVALID_ARG, "score_topk: misaligned pointer");
+  if (!std::isfinite(gamma) || !std::isfinite(tau_rel) || tau_rel < 0)
+    return fail(KVSEL_ERR_INVALID_ARG, "score_topk: gamma and tau_rel must be finite, tau_rel >= 0");
+  if (!ws || ws_bytes < score_topk_ws_bytes(*p) || !aligned16(ws))
+    return fail(KVSEL_ERR_WORKSPACE, "score_topk: workspace missing, small or misaligned");
+  int* ew = device_error_word();
+  if (!ew) return fail(KVSEL_ERR_CUDA, "score_topk: no CUDA device");
+  return cuda_status(launch_score_topk(*p, q, summaries, seq_lens, k_per_seq, gamma, tau_rel,
+                                       sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
+                                       scores_out, ws, ew, reinterpret_cast<cudaStream_t>(stream)),
+                     "score_topk launch");
+}
+
+int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, const int32_t* n_sel,
+                      int32_t* span_start, int32_t* span_len, int32_t* n_spans,
+                      kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  if (p->batch == 0) return KVSEL_OK;
+  if (!sel_idx || !n_sel || !span_start || !span_len || !n_spans)
+    return fail(KVSEL_ERR_INVALID_ARG, "merge_spans: NULL pointer");
+  int* ew = device_error_word();
+  if (!ew) return fail(KVSEL_ERR_CUDA, "merge_spans: no CUDA device");
+  return cuda_status(launch_merge_spans(*p, sel_idx, n_sel, span_start, span_len, n_spans, ew,
+                                        reinterpret_cast<cudaStream_t>(stream)),
+                     "merge_spans launch");
+}
+
+static int check_host_kv(const kvsel_problem* p, const kvsel_kv_src* kv, const void** dev_ptr) {
+  if (!kv->host_kv || !kv->staging || kv->staging_slots <= 0 || kv->host_blocks <= 0)
+    return fail(KVSEL_ERR_INVALID_ARG, "host tier: host_kv, staging, slots and host_blocks required");
+  if (!aligned16(kv->host_kv) || !aligned16(kv->staging))
+    return fail(KVSEL_ERR_INVALID_ARG, "host tier: misaligned pointer");
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, kv->host_kv) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(KVSEL_ERR_INVALID_ARG, "host tier: host_kv is not known to CUDA (pin it)");
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr)
+    return fail(KVSEL_ERR_INVALID_ARG, "host tier: host_kv is not device-mapped pinned memory");
+  *dev_ptr = at.devicePointer;
+  const int64_t rows = int64_t(p->batch) * kv->staging_slots * 2 * p->n_kvheads * p->block_size;
+  if (rows >= (int64_t(1) << 31))
+    return fail(KVSEL_ERR_UNSUPPORTED, "host tier: staging larger than 2^31 rows");
+  return KVSEL_OK;
+}
+
+int kvsel_fetch_spans(const kvsel_problem* p, const kvsel_kv_src* kv, const int32_t* seq_lens,
+                      const int32_t* span_start, const int32_t* span_len,
+                      const int32_t* n_spans, const uint8_t* dense_flag,
+                      kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  if (!kv || kv->kind != KVSEL_KV_HOST)
+    return fail(KVSEL_ERR_INVALID_ARG, "fetch_spans: kv source must be KVSEL_KV_HOST");
+  if (p->batch == 0) return KVSEL_OK;
+  if (!seq_lens || !span_start || !span_len || !n_spans)
+    return fail(KVSEL_ERR_INVALID_ARG, "fetch_spans: NULL pointer");
+  const void* dev_host = nullptr;
+  r = check_host_kv(p, kv, &dev_host);
+  if (r) return r;
+  kvsel_kv_src k2 = *kv;
+  k2.host_kv = static_cast<const kvsel_bf16*>(dev_host);
+  int* ew = device_error_word();
+  if (!ew) return fail(KVSEL_ERR_CUDA, "fetch_spans: no CUDA device");
+  return cuda_status(launch_fetch_spans(*p, k2, seq_lens, span_start, span_len, n_spans,
+                                        dense_flag, ew, reinterpret_cast<cudaStream_t>(stream)),
+                     "fetch_spans launch");
+}
+
+int kvsel_sparse_decode(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_kv_src* kv,
+                        const int32_t* seq_lens, const int32_t* sel_idx, const int32_t* n_sel,
+                        const int32_t* span_start, const int32_t* span_len,
+                        const int32_t* n_spans, const uint8_t* dense_flag, float softmax_scale,
+                        float* out, kvsel_bf16* out_bf16, float* lse, void* ws,
+                        size_t ws_bytes, kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  if (!kv) return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: kv is NULL");
+  if (p->batch == 0) return KVSEL_OK;
+  if (!q || !seq_lens || !sel_idx || !n_sel || !out || !lse)
+    return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: NULL pointer");
+  if (!aligned16(q) || !aligned16(out) || !aligned4(lse) || !aligned4(sel_idx) ||
+      !aligned4(n_sel) || !aligned4(seq_lens) || (out_bf16 && !aligned16(out_bf16)))
+    return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: misaligned pointer");
+  if (!std::isfinite(softmax_scale))
+    return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: softmax_scale must be finite");
+  if (!ws || ws_bytes < sparse_decode_ws_bytes(*p) || !aligned16(ws))
+    return fail(KVSEL_ERR_WORKSPACE, "sparse_decode: workspace missing, small or misaligned");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* ew = device_error_word();
+  if (!ew) return fail(KVSEL_ERR_CUDA, "sparse_decode: no CUDA device");
+  kvsel_kv_src src = *kv;
+  if (kv->kind == KVSEL_KV_PAGED) {
+    if (!kv->k_pages || !kv->v_pages || !kv->block_table || kv->n_pages <= 0)
+      return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: paged source needs pages and a block table");
+    if (!aligned16(kv->k_pages) || !aligned16(kv->v_pages))
+      return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: misaligned pages");
+    if (kv->n_pages * p->n_kvheads * p->block_size >= (int64_t(1) << 31))
+      return fail(KVSEL_ERR_UNSUPPORTED, "sparse_decode: more than 2^31 cache rows");
+  } else if (kv->kind == KVSEL_KV_STAGED || kv->kind == KVSEL_KV_HOST) {
+    if (kv->kind == KVSEL_KV_HOST) {
+      if (!span_start || !span_len || !n_spans)
+        return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: host source needs the spans");
+      const void* dev_host = nullptr;
+      r = check_host_kv(p, kv, &dev_host);
+      if (r) return r;
+      src.host_kv = static_cast<const kvsel_bf16*>(dev_host);
+      r = cuda_status(launch_fetch_spans(*p, src, seq_lens, span_start, span_len, n_spans,
+                                         dense_flag, ew, s),
+                      "sparse_decode fetch launch");
+      if (r) return r;
+    }
+    if (!kv->staging || kv->staging_slots <= 0 || !aligned16(kv->staging))
+      return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: staging buffer and slots required");
+    if (int64_t(p->batch) * kv->staging_slots * 2 * p->n_kvheads * p->block_size >= (int64_t(1) << 31))
+      return fail(KVSEL_ERR_UNSUPPORTED, "sparse_decode: staging larger than 2^31 rows");
+    src.kind = KVSEL_KV_STAGED;
+  } else {
+    return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: unknown kv kind");
+  }
+  return cuda_status(launch_sparse_decode(*p, q, src, seq_lens, sel_idx, n_sel, dense_flag,
+                                          softmax_scale, out, out_bf16, lse, ws, ew, s),
+                     "sparse_decode launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Host-side launchers shared between the C-ABI layer (api.cu) and the kernel
+// translation units. Arguments are validated by the caller before a launcher
+// runs; launchers only size grids and enqueue work.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvsel.h"
+
+namespace kvsel {
+
+// Per-device error word (device address) and launch counter.
+int* device_error_word();
+void count_launch(int n = 1);
+int sm_count();
+void set_last_error(const char* fmt, ...);
+
+// ---- summaries (summaries.cu) ----
+cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16* k_pages,
+                                   kvsel_bf16* v_pages, int64_t n_pages, const int32_t* block_table,
+                                   const int32_t* seq_lens, const int32_t* append_pos,
+                                   const kvsel_bf16* new_k, const kvsel_bf16* new_v,
+                                   kvsel_bf16* summaries, double* open_acc, int* err,
+                                   cudaStream_t s);
+
+// ---- score + Top-k + spans (score_topk.cu) ----
+size_t score_topk_ws_bytes(const kvsel_problem& p);
+cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
+                              const kvsel_bf16* summaries, const int32_t* seq_lens,
+                              const int32_t* k_per_seq, float gamma, float tau_rel,
+                              int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                              int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                              float* scores_out, void* ws, int* err, cudaStream_t s);
+cudaError_t launch_merge_spans(const kvsel_problem& p, const int32_t* sel_idx,
+                               const int32_t* n_sel, int32_t* span_start, int32_t* span_len,
+                               int32_t* n_spans, int* err, cudaStream_t s);
+
+// ---- sparse decode (sparse_decode.cu) ----
+size_t sparse_decode_ws_bytes(const kvsel_problem& p);
+cudaError_t launch_sparse_decode(const kvsel_problem& p, const kvsel_bf16* q,
+                                 const kvsel_kv_src& kv, const int32_t* seq_lens,
+                                 const int32_t* sel_idx, const int32_t* n_sel,
+                                 const uint8_t* dense_flag, float softmax_scale, float* out,
+                                 kvsel_bf16* out_bf16, float* lse, void* ws, int* err,
+                                 cudaStream_t s);
+
+// ---- offload tier (offload.cu) ----
+cudaError_t launch_fetch_spans(const kvsel_problem& p, const kvsel_kv_src& kv,
+                               const int32_t* seq_lens, const int32_t* span_start,
+                               const int32_t* span_len, const int32_t* n_spans,
+                               const uint8_t* dense_flag, int* err, cudaStream_t s);
+
+}  // namespace kvsel

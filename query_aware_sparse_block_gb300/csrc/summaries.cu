@@ -1,0 +1,188 @@
+// Block summaries: the mean key of every KV block, one vector per KV head
+// ("SparPR KV cache recovery on a consumer GPU", paragraph "Query-Aware
+// key-block selection": a compact precomputed summary per block, resident on
+// the GPU), plus the incremental update as decode appends tokens.
+//
+// Arithmetic: each summary element is the fp64 sum of the block's keys taken
+// in token order from +0.0, divided by the token count in fp64 and rounded
+// once to bf16 (nearest, ties to even). The rounding from fp64 goes through
+// fp32 with round-to-odd, which gives the same result as one direct rounding
+// whenever the intermediate format carries at least two more bits than the
+// target (Boldo and Melquiond, "Emulation of FMA and correctly rounded sums:
+// proved algorithms using rounding to odd", IEEE Trans. Computers, 2008);
+// fp32 carries 24 bits against bf16's 8.
+#include "kvsel_common.cuh"
+#include "kvsel_internal.h"
+
+namespace kvsel {
+namespace {
+
+constexpr int kThreads = 128;
+
+__device__ __forceinline__ uint16_t f64_to_bf16_rne(double x) {
+  float f = __double2float_rz(x);
+  if (static_cast<double>(f) != x) f = __uint_as_float(__float_as_uint(f) | 1u);  // round to odd
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, double (&x)[8]) {
+  x[0] = bf16lo(v.x); x[1] = bf16hi(v.x);
+  x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
+  x[4] = bf16lo(v.z); x[5] = bf16hi(v.z);
+  x[6] = bf16lo(v.w); x[7] = bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint4 mean_to_bf16x8(const double (&acc)[8], int cnt) {
+  const double c = static_cast<double>(cnt);
+  uint16_t h[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) h[i] = f64_to_bf16_rne(acc[i] / c);
+  uint4 r;
+  r.x = h[0] | (uint32_t(h[1]) << 16);
+  r.y = h[2] | (uint32_t(h[3]) << 16);
+  r.z = h[4] | (uint32_t(h[5]) << 16);
+  r.w = h[6] | (uint32_t(h[7]) << 16);
+  return r;
+}
+
+// One CTA per (block n, sequence b). Threads own 8-channel column vectors of
+// one KV head and walk the block's tokens in order.
+__global__ void __launch_bounds__(kThreads) summaries_full_kernel(
+    const kvsel_bf16* __restrict__ k_pages, int64_t n_pages, const int32_t* __restrict__ block_table,
+    const int32_t* __restrict__ seq_lens, kvsel_bf16* __restrict__ summaries,
+    double* __restrict__ open_acc, int H, int d, int B, int max_blocks, int* err) {
+  const int n = blockIdx.x;
+  const int b = blockIdx.y;
+  int T = seq_lens[b];
+  if (T < 0 || T > max_blocks * B) {
+    if (n == 0 && threadIdx.x == 0) latch_error(err, KVSEL_ERR_BOUNDS);
+    T = T < 0 ? 0 : max_blocks * B;
+  }
+  const int N = (T + B - 1) / B;
+  const int vec_per_head = d / 8;
+  const int n_vec = H * vec_per_head;
+  if (N == 0) {
+    if (n == 0)
+      for (int i = threadIdx.x; i < H * d; i += blockDim.x) open_acc[int64_t(b) * H * d + i] = 0.0;
+    return;
+  }
+  if (n >= N) return;
+  const int64_t page = block_table[int64_t(b) * max_blocks + n];
+  if (page < 0 || page >= n_pages) {
+    if (threadIdx.x == 0) latch_error(err, KVSEL_ERR_BOUNDS);
+    return;
+  }
+  const int cnt = min(B, T - n * B);
+  for (int v = threadIdx.x; v < n_vec; v += blockDim.x) {
+    const int j = v / vec_per_head;
+    const int c0 = (v % vec_per_head) * 8;
+    const kvsel_bf16* src = k_pages + ((page * H + j) * B) * int64_t(d) + c0;
+    double acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.0;
+    int t = 0;
+    for (; t + 8 <= cnt; t += 8) {
+      uint4 r[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) r[u] = ldg_stream(src + int64_t(t + u) * d);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        double x[8];
+        unpack8(r[u], x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += x[i];
+      }
+    }
+    for (; t < cnt; ++t) {
+      double x[8];
+      unpack8(ldg_stream(src + int64_t(t) * d), x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += x[i];
+    }
+    const int64_t so = ((int64_t(b) * max_blocks + n) * H + j) * d + c0;
+    *reinterpret_cast<uint4*>(summaries + so) = mean_to_bf16x8(acc, cnt);
+    if (n == N - 1) {
+      double* oa = open_acc + (int64_t(b) * H + j) * d + c0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) oa[i] = acc[i];
+    }
+  }
+}
+
+// One CTA per sequence: write the new token (optional), fold it into the open
+// block's fp64 accumulator and rewrite that block's summary.
+__global__ void __launch_bounds__(kThreads) summaries_append_kernel(
+    kvsel_bf16* __restrict__ k_pages, kvsel_bf16* __restrict__ v_pages, int64_t n_pages,
+    const int32_t* __restrict__ block_table, const int32_t* __restrict__ append_pos,
+    const kvsel_bf16* __restrict__ new_k, const kvsel_bf16* __restrict__ new_v,
+    kvsel_bf16* __restrict__ summaries, double* __restrict__ open_acc, int H, int d, int B,
+    int max_blocks, int* err) {
+  const int b = blockIdx.x;
+  const int t = append_pos[b];
+  if (t < 0) return;
+  if (t >= max_blocks * B) {
+    if (threadIdx.x == 0) latch_error(err, KVSEL_ERR_BOUNDS);
+    return;
+  }
+  const int n = t / B;
+  const int row = t % B;
+  const int64_t page = block_table[int64_t(b) * max_blocks + n];
+  if (page < 0 || page >= n_pages) {
+    if (threadIdx.x == 0) latch_error(err, KVSEL_ERR_BOUNDS);
+    return;
+  }
+  const int vec_per_head = d / 8;
+  const int n_vec = H * vec_per_head;
+  for (int v = threadIdx.x; v < n_vec; v += blockDim.x) {
+    const int j = v / vec_per_head;
+    const int c0 = (v % vec_per_head) * 8;
+    const int64_t cache_off = ((page * H + j) * B + row) * int64_t(d) + c0;
+    const int64_t tok_off = (int64_t(b) * H + j) * d + c0;
+    uint4 kv;
+    if (new_k) {
+      kv = *reinterpret_cast<const uint4*>(new_k + tok_off);
+      *reinterpret_cast<uint4*>(k_pages + cache_off) = kv;
+      if (new_v && v_pages)
+        *reinterpret_cast<uint4*>(v_pages + cache_off) =
+            *reinterpret_cast<const uint4*>(new_v + tok_off);
+    } else {
+      kv = *reinterpret_cast<const uint4*>(k_pages + cache_off);
+    }
+    double x[8];
+    unpack8(kv, x);
+    double* oa = open_acc + tok_off;
+    double acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      acc[i] = (row == 0 ? 0.0 : oa[i]) + x[i];
+      oa[i] = acc[i];
+    }
+    const int64_t so = ((int64_t(b) * max_blocks + n) * H + j) * d + c0;
+    *reinterpret_cast<uint4*>(summaries + so) = mean_to_bf16x8(acc, row + 1);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16* k_pages,
+                                   kvsel_bf16* v_pages, int64_t n_pages, const int32_t* block_table,
+                                   const int32_t* seq_lens, const int32_t* append_pos,
+                                   const kvsel_bf16* new_k, const kvsel_bf16* new_v,
+                                   kvsel_bf16* summaries, double* open_acc, int* err,
+                                   cudaStream_t s) {
+  if (p.batch == 0) return cudaSuccess;
+  if (mode == KVSEL_SUMMARY_FULL) {
+    dim3 grid(p.max_blocks, p.batch);
+    summaries_full_kernel<<<grid, kThreads, 0, s>>>(k_pages, n_pages, block_table, seq_lens,
+                                                    summaries, open_acc, p.n_kvheads, p.head_dim,
+                                                    p.block_size, p.max_blocks, err);
+  } else {
+    summaries_append_kernel<<<p.batch, kThreads, 0, s>>>(
+        k_pages, v_pages, n_pages, block_table, append_pos, new_k, new_v, summaries, open_acc,
+        p.n_kvheads, p.head_dim, p.block_size, p.max_blocks, err);
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace kvsel

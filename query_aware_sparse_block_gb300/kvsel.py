@@ -1,0 +1,283 @@
+"""ctypes binding of libkvsel.so (argument marshalling only).
+
+Every function here forwards torch tensors' device pointers and the current
+CUDA stream to the C entry point of the same name in ``include/kvsel.h``; all
+compute runs in the library's CUDA kernels. There is no fallback: if the
+library is missing or a call fails, a ``KvselError`` is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvsel.so")
+
+KVSEL_OK = 0
+KVSEL_ERR_INVALID_ARG = 1
+KVSEL_ERR_CUDA = 2
+KVSEL_ERR_BOUNDS = 3
+KVSEL_ERR_TIMEOUT = 4
+KVSEL_ERR_UNSUPPORTED = 5
+KVSEL_ERR_WORKSPACE = 6
+
+KVSEL_SUMMARY_FULL = 0
+KVSEL_SUMMARY_APPEND = 1
+KVSEL_KV_PAGED = 0
+KVSEL_KV_STAGED = 1
+KVSEL_KV_HOST = 2
+KVSEL_WS_SCORE_TOPK = 0
+KVSEL_WS_SPARSE_DECODE = 1
+
+_STATUS = {1: "INVALID_ARG", 2: "CUDA", 3: "BOUNDS", 4: "TIMEOUT", 5: "UNSUPPORTED", 6: "WORKSPACE"}
+
+
+class KvselError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str = ""):
+        self.code = code
+        super().__init__(f"{where}: KVSEL_ERR_{_STATUS.get(code, code)} {detail}".rstrip())
+
+
+class kvsel_problem(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_qheads", ctypes.c_int32),
+                ("n_kvheads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("max_blocks", ctypes.c_int32),
+                ("k_max", ctypes.c_int32)]
+
+
+class kvsel_kv_src(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("staging_slots", ctypes.c_int32),
+                ("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p),
+                ("block_table", ctypes.c_void_p), ("n_pages", ctypes.c_int64),
+                ("staging", ctypes.c_void_p), ("host_kv", ctypes.c_void_p),
+                ("host_blocks", ctypes.c_int32), ("fetch_ctas", ctypes.c_int32)]
+
+
+class kvsel_budget_in(ctypes.Structure):
+    _fields_ = [("block_size", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("elem_bytes", ctypes.c_int32),
+                ("hidden", ctypes.c_int64), ("n_blocks", ctypes.c_int64),
+                ("h2d_bytes_per_s", ctypes.c_double), ("recompute_flop_per_s", ctypes.c_double),
+                ("kappa", ctypes.c_double), ("keep_floor", ctypes.c_double),
+                ("gamma", ctypes.c_double), ("tau_s", ctypes.c_double),
+                ("keep_override", ctypes.c_double)]
+
+
+class kvsel_budget_out(ctypes.Structure):
+    _fields_ = [("c_copy_s", ctypes.c_double), ("c_rec_s", ctypes.c_double),
+                ("r_model", ctypes.c_double), ("r", ctypes.c_double), ("k", ctypes.c_int64),
+                ("tau_rel", ctypes.c_double), ("dense", ctypes.c_int32)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "kvsel_build_summaries": (_I, [ctypes.POINTER(kvsel_problem), _I, _P, _P, ctypes.c_int64, _P, _P,
+                                   _P, _P, _P, _P, _P, _P]),
+    "kvsel_score_topk": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, ctypes.c_float,
+                              ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "kvsel_merge_spans": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, _P, _P]),
+    "kvsel_sparse_decode": (_I, [ctypes.POINTER(kvsel_problem), _P, ctypes.POINTER(kvsel_kv_src), _P,
+                                 _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
+                                 ctypes.c_size_t, _P]),
+    "kvsel_fetch_spans": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_kv_src), _P, _P, _P,
+                               _P, _P, _P]),
+    "kvsel_budget": (_I, [ctypes.POINTER(kvsel_budget_in), ctypes.POINTER(kvsel_budget_out)]),
+    "kvsel_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kvsel_problem), _I]),
+    "kvsel_kv_bytes_per_token": (ctypes.c_int64, [ctypes.c_int32] * 4),
+    "kvsel_get_error": (_I, [_P]),
+    "kvsel_launch_count": (ctypes.c_uint64, []),
+    "kvsel_last_error": (ctypes.c_char_p, []),
+    "kvsel_version": (ctypes.c_char_p, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                        "(nvcc, sm_103a); there is no non-CUDA fallback")
+                L = ctypes.CDLL(LIB_PATH)
+                for name, (res, args) in _SIGS.items():
+                    fn = getattr(L, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = L
+    return _lib
+
+
+def _check(code: int, where: str):
+    if code != KVSEL_OK:
+        detail = lib().kvsel_last_error().decode(errors="replace")
+        raise KvselError(code, where, detail)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def problem(batch, n_qheads, n_kvheads, head_dim, block_size, max_blocks, k_max=None) -> kvsel_problem:
+    return kvsel_problem(int(batch), int(n_qheads), int(n_kvheads), int(head_dim), int(block_size),
+                         int(max_blocks), int(k_max if k_max is not None else max_blocks))
+
+
+def _expect(t, dtype, name, cuda=True):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise TypeError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+
+
+# ------------------------------------------------------------ entry points ---
+
+def kvsel_version() -> str:
+    return lib().kvsel_version().decode()
+
+
+def kvsel_launch_count() -> int:
+    return int(lib().kvsel_launch_count())
+
+
+def kvsel_kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes) -> int:
+    return int(lib().kvsel_kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes))
+
+
+def kvsel_workspace_size(p: kvsel_problem, which: int) -> int:
+    return int(lib().kvsel_workspace_size(ctypes.byref(p), which))
+
+
+def kvsel_budget(block_size, kv_heads, head_dim, elem_bytes, hidden, n_blocks, h2d_bytes_per_s,
+                 recompute_flop_per_s, kappa=2.0, keep_floor=0.0, gamma=1.0, tau_s=0.0,
+                 keep_override=-1.0) -> kvsel_budget_out:
+    i = kvsel_budget_in(block_size, kv_heads, head_dim, elem_bytes, hidden, n_blocks,
+                        h2d_bytes_per_s, recompute_flop_per_s, kappa, keep_floor, gamma, tau_s,
+                        keep_override)
+    o = kvsel_budget_out()
+    _check(lib().kvsel_budget(ctypes.byref(i), ctypes.byref(o)), "kvsel_budget")
+    return o
+
+
+def kvsel_get_error(stream=None) -> int:
+    return int(lib().kvsel_get_error(_stream(stream)))
+
+
+def kvsel_build_summaries(p, mode, k_pages, v_pages, block_table, seq_lens, summaries, open_acc,
+                          append_pos=None, new_k=None, new_v=None, stream=None):
+    for t, dt, n in ((k_pages, torch.bfloat16, "k_pages"), (v_pages, torch.bfloat16, "v_pages"),
+                     (block_table, torch.int32, "block_table"), (seq_lens, torch.int32, "seq_lens"),
+                     (summaries, torch.bfloat16, "summaries"), (open_acc, torch.float64, "open_acc"),
+                     (append_pos, torch.int32, "append_pos"), (new_k, torch.bfloat16, "new_k"),
+                     (new_v, torch.bfloat16, "new_v")):
+        _expect(t, dt, n)
+    _check(lib().kvsel_build_summaries(ctypes.byref(p), mode, _ptr(k_pages), _ptr(v_pages),
+                                       k_pages.shape[0], _ptr(block_table), _ptr(seq_lens),
+                                       _ptr(append_pos), _ptr(new_k), _ptr(new_v), _ptr(summaries),
+                                       _ptr(open_acc), _stream(stream)),
+           "kvsel_build_summaries")
+
+
+def kvsel_score_topk(p, q, summaries, seq_lens, k_per_seq, sel_idx, n_sel, span_start, span_len,
+                     n_spans, ws, gamma=2.0, tau_rel=0.0, dense_flag=None, scores_out=None,
+                     stream=None):
+    for t, dt, n in ((q, torch.bfloat16, "q"), (summaries, torch.bfloat16, "summaries"),
+                     (seq_lens, torch.int32, "seq_lens"), (k_per_seq, torch.int32, "k_per_seq"),
+                     (sel_idx, torch.int32, "sel_idx"), (n_sel, torch.int32, "n_sel"),
+                     (span_start, torch.int32, "span_start"), (span_len, torch.int32, "span_len"),
+                     (n_spans, torch.int32, "n_spans"), (dense_flag, torch.uint8, "dense_flag"),
+                     (scores_out, torch.float32, "scores_out")):
+        _expect(t, dt, n)
+    _check(lib().kvsel_score_topk(ctypes.byref(p), _ptr(q), _ptr(summaries), _ptr(seq_lens),
+                                  _ptr(k_per_seq), float(gamma), float(tau_rel), _ptr(sel_idx),
+                                  _ptr(n_sel), _ptr(span_start), _ptr(span_len), _ptr(n_spans),
+                                  _ptr(dense_flag), _ptr(scores_out), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream)),
+           "kvsel_score_topk")
+
+
+def kvsel_merge_spans(p, sel_idx, n_sel, span_start, span_len, n_spans, stream=None):
+    for t, n in ((sel_idx, "sel_idx"), (n_sel, "n_sel"), (span_start, "span_start"),
+                 (span_len, "span_len"), (n_spans, "n_spans")):
+        _expect(t, torch.int32, n)
+    _check(lib().kvsel_merge_spans(ctypes.byref(p), _ptr(sel_idx), _ptr(n_sel), _ptr(span_start),
+                                   _ptr(span_len), _ptr(n_spans), _stream(stream)),
+           "kvsel_merge_spans")
+
+
+def kv_paged(k_pages, v_pages, block_table) -> kvsel_kv_src:
+    _expect(k_pages, torch.bfloat16, "k_pages")
+    _expect(v_pages, torch.bfloat16, "v_pages")
+    _expect(block_table, torch.int32, "block_table")
+    s = kvsel_kv_src()
+    s.kind = KVSEL_KV_PAGED
+    s.k_pages, s.v_pages, s.block_table = _ptr(k_pages), _ptr(v_pages), _ptr(block_table)
+    s.n_pages = k_pages.shape[0]
+    return s
+
+
+def kv_staged(staging, slots) -> kvsel_kv_src:
+    _expect(staging, torch.bfloat16, "staging")
+    s = kvsel_kv_src()
+    s.kind = KVSEL_KV_STAGED
+    s.staging, s.staging_slots = _ptr(staging), int(slots)
+    return s
+
+
+def kv_host(host_kv, host_blocks, staging, slots, fetch_ctas=0) -> kvsel_kv_src:
+    _expect(host_kv, torch.bfloat16, "host_kv", cuda=False)
+    _expect(staging, torch.bfloat16, "staging")
+    if not host_kv.is_pinned():
+        raise ValueError("host_kv must be pinned host memory")
+    s = kvsel_kv_src()
+    s.kind = KVSEL_KV_HOST
+    s.host_kv, s.host_blocks = _ptr(host_kv), int(host_blocks)
+    s.staging, s.staging_slots, s.fetch_ctas = _ptr(staging), int(slots), int(fetch_ctas)
+    return s
+
+
+def kvsel_sparse_decode(p, q, kv: kvsel_kv_src, seq_lens, sel_idx, n_sel, out, lse, ws,
+                        softmax_scale, dense_flag=None, span_start=None, span_len=None,
+                        n_spans=None, out_bf16=None, stream=None):
+    for t, dt, n in ((q, torch.bfloat16, "q"), (seq_lens, torch.int32, "seq_lens"),
+                     (sel_idx, torch.int32, "sel_idx"), (n_sel, torch.int32, "n_sel"),
+                     (out, torch.float32, "out"), (lse, torch.float32, "lse"),
+                     (dense_flag, torch.uint8, "dense_flag"), (out_bf16, torch.bfloat16, "out_bf16")):
+        _expect(t, dt, n)
+    _check(lib().kvsel_sparse_decode(ctypes.byref(p), _ptr(q), ctypes.byref(kv), _ptr(seq_lens),
+                                     _ptr(sel_idx), _ptr(n_sel), _ptr(span_start), _ptr(span_len),
+                                     _ptr(n_spans), _ptr(dense_flag), float(softmax_scale),
+                                     _ptr(out), _ptr(out_bf16), _ptr(lse), _ptr(ws),
+                                     ws.numel() * ws.element_size(), _stream(stream)),
+           "kvsel_sparse_decode")
+
+
+def kvsel_fetch_spans(p, kv: kvsel_kv_src, seq_lens, span_start, span_len, n_spans,
+                      dense_flag=None, stream=None):
+    _check(lib().kvsel_fetch_spans(ctypes.byref(p), ctypes.byref(kv), _ptr(seq_lens),
+                                   _ptr(span_start), _ptr(span_len), _ptr(n_spans),
+                                   _ptr(dense_flag), _stream(stream)),
+           "kvsel_fetch_spans")

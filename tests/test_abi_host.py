@@ -1,0 +1,119 @@
+"""CPU-side checks of the C ABI: the library builds and loads, exports every
+function include/kvsel.h declares, and its host-only logic (budget, KV bytes,
+argument validation, workspace sizing) agrees with the oracle and the pages.
+No compute call is made here (no GPU)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle as o
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def K():
+    from query_aware_sparse_block_gb300.build import build_library
+    build_library()
+    from query_aware_sparse_block_gb300 import kvsel
+    kvsel.lib()
+    return kvsel
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "kvsel.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"KVSEL_API\s+[\w\s\*]+?\b(kvsel_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("kvsel_build_summaries", "kvsel_score_topk", "kvsel_merge_spans",
+              "kvsel_sparse_decode", "kvsel_budget", "kvsel_fetch_spans",
+              "kvsel_workspace_size", "kvsel_kv_bytes_per_token", "kvsel_get_error",
+              "kvsel_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(K):
+    L = ctypes.CDLL(K.LIB_PATH)
+    for n in _declared_functions():
+        assert hasattr(L, n), n
+    assert K.kvsel_version().startswith("kvsel")
+
+
+def test_kv_bytes_per_token_matches_worked_example(K):
+    assert K.kvsel_kv_bytes_per_token(32, 2, 128, 2) == 32768
+    assert K.kvsel_kv_bytes_per_token(40, 40, 128, 2) == 819200
+    assert K.kvsel_kv_bytes_per_token(-1, 2, 128, 2) == -1
+
+
+def _golden_budget_rows():
+    path = os.path.join(ROOT, "tests", "golden", "budget_hand_examples.txt")
+    rows = []
+    with open(path) as f:
+        for ln in f:
+            if ln.strip() and not ln.startswith("#"):
+                rows.append(ln.split("|")[0].split())
+    return rows
+
+
+def test_budget_equals_oracle_bit_for_bit(K):
+    rows = _golden_budget_rows()
+    extra = [["16", "32", "128", "2", "4096", "256", "12e9", "80e12", "2", "0.05", "0.8", "0", "-1"],
+             ["64", "2", "128", "2", "4096", "2048", "3.9e11", "1.7376e15", "2", "0.05", "0.8", "0", "-1"],
+             ["32", "8", "128", "2", "2560", "1024", "6.7e12", "1.7e15", "2", "0", "1", "1e-7", "0.125"]]
+    for r in rows + extra:
+        B, H, d, e, hid, N = map(int, r[:6])
+        bw, F, kappa, floor, gamma, tau, ovr = map(float, r[6:])
+        got = K.kvsel_budget(B, H, d, e, hid, N, bw, F, kappa, floor, gamma, tau, ovr)
+        want = o.budget(B, H, d, e, hid, N, bw, F, kappa, floor, gamma, tau, ovr)
+        assert got.c_copy_s == want.c_copy_s
+        assert got.c_rec_s == want.c_rec_s
+        assert got.r_model == want.r_model
+        assert got.r == want.r
+        assert got.k == want.k
+        assert got.tau_rel == want.tau_rel
+        assert bool(got.dense) == want.dense
+
+
+def test_budget_rejects_bad_input(K):
+    with pytest.raises(K.KvselError) as ei:
+        K.kvsel_budget(64, 2, 128, 2, 4096, 10, 0.0, 1e15)
+    assert ei.value.code == K.KVSEL_ERR_INVALID_ARG
+
+
+def test_workspace_sizes_and_shape_validation(K):
+    p = K.problem(16, 32, 8, 128, 32, 1028, 1028)
+    assert K.kvsel_workspace_size(p, K.KVSEL_WS_SCORE_TOPK) >= 16 * 1028 * 4
+    assert K.kvsel_workspace_size(p, K.KVSEL_WS_SPARSE_DECODE) > 0
+    for bad in (K.problem(1, 8, 8, 96, 16, 64), K.problem(1, 8, 3, 64, 16, 64),
+                K.problem(1, 64, 2, 128, 16, 64), K.problem(1, 8, 8, 64, 48, 64),
+                K.problem(1, 8, 8, 64, 16, 0), K.problem(5000, 8, 8, 64, 16, 64),
+                K.problem(1, 8, 8, 64, 16, 64, 65)):
+        assert K.kvsel_workspace_size(bad, K.KVSEL_WS_SCORE_TOPK) == 0
+
+
+def test_entry_points_validate_before_touching_the_device(K):
+    bad = K.problem(1, 8, 8, 96, 16, 64)    # head_dim 96 is not compiled
+    L = K.lib()
+    rc = L.kvsel_score_topk(ctypes.byref(bad), None, None, None, None, 1.0, 0.0, None, None, None,
+                            None, None, None, None, None, 0, None)
+    assert rc == K.KVSEL_ERR_UNSUPPORTED
+    good = K.problem(1, 8, 8, 64, 16, 64)
+    rc = L.kvsel_score_topk(ctypes.byref(good), None, None, None, None, 1.0, 0.0, None, None, None,
+                            None, None, None, None, None, 0, None)
+    assert rc == K.KVSEL_ERR_INVALID_ARG
+    src = K.kvsel_kv_src()
+    src.kind = 7
+    rc = L.kvsel_sparse_decode(ctypes.byref(good), None, ctypes.byref(src), None, None, None, None,
+                               None, None, None, 0.125, None, None, None, None, 0, None)
+    assert rc == K.KVSEL_ERR_INVALID_ARG
+    rc = L.kvsel_build_summaries(ctypes.byref(good), 9, None, None, 0, None, None, None, None, None,
+                                 None, None, None)
+    assert rc == K.KVSEL_ERR_INVALID_ARG
+    assert b"mode" in L.kvsel_last_error()

@@ -113,6 +113,5 @@ def host_tier_layout(k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: 
         out = torch.empty((b, n_blocks, 2, Hkv, B, d), dtype=torch.bfloat16)
     for s in range(b):
         p = block_table[s, :n_blocks].long().to(k_pages.device)
-        out[s, :, 0].copy_(k_pages[p])
-        out[s, :, 1].copy_(v_pages[p])
+        out[s].copy_(torch.stack([k_pages[p], v_pages[p]], dim=1))
     return out
