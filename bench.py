@@ -44,13 +44,13 @@ UNIT = "layer-steps/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvsel", choices=["kvsel", "reference"])
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (debug)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--ref-seqs", type=int, default=2, help="sequences per oracle sample")
+    ap.add_argument("--ref-seqs", type=int, default=4, help="sequences per oracle sample")
     return ap.parse_args()
 
 
@@ -88,7 +88,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -139,14 +139,16 @@ class Workbench:
 
         self.w, self.L, self.device = w, layers, device
         B = w.block_size
-        self.T0 = w.seq_len
-        self.max_blocks = (self.T0 + total_steps + B - 1) // B + 1
+        # the last step ends with exactly seq_len cached tokens
+        self.T0 = w.seq_len - total_steps
+        self.max_blocks = (w.seq_len + B - 1) // B
         self.k = w.k_for(w.keep[0])
         self.dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, B, self.max_blocks,
                                  k_max=self.k, device=device)
         self.layers = []
         for l in range(layers):
-            x = generate_layer(w, l, device=device, max_blocks=self.max_blocks, perm=False)
+            x = generate_layer(w, l, device=device, max_blocks=self.max_blocks, perm=False,
+                               seq_lens=[self.T0] * w.batch)
             summ, acc = self.dec.new_summaries()
             self.dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
             g = torch.Generator(device=device)
@@ -165,11 +167,19 @@ class Workbench:
         self.seq_lens = self.append_pos + 1
         self.dec.k_per_seq.fill_(self.k)
         self.step_i = 0
-        self.kv_src = [None] * layers
         from query_aware_sparse_block_gb300 import kvsel as K
+        from query_aware_sparse_block_gb300.runtime import BoundLayer
+        import ctypes
         self.K = K
-        for l, d in enumerate(self.layers):
-            self.kv_src[l] = K.kv_paged(d["x"]["k_pages"], d["x"]["v_pages"], d["x"]["block_table"])
+        self.bound = [BoundLayer(self.dec, d["x"]["q"], d["x"]["k_pages"], d["x"]["v_pages"],
+                                 d["x"]["block_table"], d["summ"], d["acc"], d["out"], d["lse"],
+                                 gamma=w.gamma, new_k=d["new_k"], new_v=d["new_v"])
+                      for d in self.layers]
+        self.pos_ptrs = [ctypes.c_void_p(self.append_pos[i].data_ptr()) for i in range(total_steps)]
+        self.len_ptrs = [ctypes.c_void_p(self.seq_lens[i].data_ptr()) for i in range(total_steps)]
+        # graph mode: one pair of device buffers advanced in place after every step
+        self.pos_buf = torch.zeros((w.batch,), dtype=torch.int32, device=device)
+        self.len_buf = torch.zeros((w.batch,), dtype=torch.int32, device=device)
 
     def budget_k(self):
         """kvsel_budget on the host: keep ratio (12.5 % override, no floor) -> k."""
@@ -179,31 +189,37 @@ class Workbench:
                                 keep_override=w.keep[0], gamma=w.gamma)
         return r
 
-    def step(self, stream, ev_score=None, ev_dec=None, q_list=None, out_list=None, nk_list=None,
-             nv_list=None):
-        """One decode step through all layers (enqueue only)."""
+    def step(self, stream, ev_score=None, ev_dec=None, q_ptrs=None, out_ptrs=None, nk_ptrs=None,
+             nv_ptrs=None, graph=False, record=None):
+        """One decode step through all layers (enqueue only). With graph=True the
+        step reads its positions from pos_buf / len_buf and advances them."""
+        import ctypes
         i = self.step_i
-        pos = self.append_pos[i]
-        lens = self.seq_lens[i]
+        if graph:
+            pos = ctypes.c_void_p(self.pos_buf.data_ptr())
+            lens = ctypes.c_void_p(self.len_buf.data_ptr())
+        else:
+            pos, lens = self.pos_ptrs[i], self.len_ptrs[i]
+        sp = ctypes.c_void_p(stream.cuda_stream)
+        rec = record or (lambda ev: ev.record(stream))
         self.budget_k()
-        for l, d in enumerate(self.layers):
-            x = d["x"]
-            q = x["q"] if q_list is None else q_list[l]
-            nk = d["new_k"] if nk_list is None else nk_list[l]
-            nv = d["new_v"] if nv_list is None else nv_list[l]
-            out = d["out"] if out_list is None else out_list[l]
-            self.dec.append(x["k_pages"], x["v_pages"], x["block_table"], pos, d["summ"], d["acc"],
-                            new_k=nk, new_v=nv, stream=stream)
+        for l, bl in enumerate(self.bound):
+            bl.append(pos, sp, None if nk_ptrs is None else nk_ptrs[l],
+                      None if nv_ptrs is None else nv_ptrs[l])
             if ev_score is not None:
-                ev_score[0][l].record(stream)
-            self.dec.select(q, d["summ"], lens, gamma=self.w.gamma, stream=stream)
+                rec(ev_score[0][l])
+            bl.select(lens, sp, None if q_ptrs is None else q_ptrs[l])
             if ev_score is not None:
-                ev_score[1][l].record(stream)
+                rec(ev_score[1][l])
             if ev_dec is not None:
-                ev_dec[0][l].record(stream)
-            self.dec.attend(q, self.kv_src[l], lens, out=out, lse=d["lse"], stream=stream)
+                rec(ev_dec[0][l])
+            bl.attend(lens, sp, None if q_ptrs is None else q_ptrs[l],
+                      None if out_ptrs is None else out_ptrs[l])
             if ev_dec is not None:
-                ev_dec[1][l].record(stream)
+                rec(ev_dec[1][l])
+        if graph:
+            self.pos_buf.add_(1)
+            self.len_buf.add_(1)
         self.step_i += 1
 
     def decode_bytes(self):
@@ -222,7 +238,28 @@ class Workbench:
         return summ + q + scores + sel
 
 
+def load_cudart():
+    """The CUDA runtime already loaded by torch (for external event records)."""
+    import ctypes
+    for name in ("libcudart.so.13", "libcudart.so.12", "libcudart.so"):
+        try:
+            lib = ctypes.CDLL(name)
+            lib.cudaEventRecordWithFlags.restype = ctypes.c_int
+            return lib
+        except OSError:
+            pass
+    with open("/proc/self/maps") as f:
+        for ln in f:
+            if "libcudart" in ln:
+                lib = ctypes.CDLL(ln.split()[-1])
+                lib.cudaEventRecordWithFlags.restype = ctypes.c_int
+                return lib
+    raise RuntimeError("libcudart not found in this process")
+
+
 def run_gpu(args):
+    import ctypes
+
     import torch
     import torch.distributed as dist
 
@@ -250,21 +287,54 @@ def run_gpu(args):
             raise RuntimeError(f"device error {err} during warm-up")
         ev_s = [[torch.cuda.Event(enable_timing=True) for _ in range(layers * args.steps)] for _ in range(2)]
         ev_d = [[torch.cuda.Event(enable_timing=True) for _ in range(layers * args.steps)] for _ in range(2)]
+        for e in ev_s[0] + ev_s[1] + ev_d[0] + ev_d[1]:
+            e.record(stream)            # creates the events before capture
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
+        # The K timed steps are captured once into a CUDA graph, so the device
+        # timing does not depend on how fast the host can enqueue. Each score and
+        # decode launch is bracketed by external event-record nodes.
+        cudart = load_cudart()
+        sp = stream.cuda_stream
+
+        def rec_ext(ev):
+            rc = cudart.cudaEventRecordWithFlags(ctypes.c_void_p(ev.cuda_event), ctypes.c_void_p(sp), 1)
+            if rc:
+                raise RuntimeError(f"cudaEventRecordWithFlags failed: {rc}")
+
+        first = wb.step_i
+        acc_snap = [d["acc"].clone() for d in wb.layers]
+
+        def reset_state():
+            wb.pos_buf.copy_(wb.append_pos[first])
+            wb.len_buf.copy_(wb.seq_lens[first])
+            for d, a in zip(wb.layers, acc_snap):
+                d["acc"].copy_(a)
+
+        reset_state()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        launches0 = K.kvsel_launch_count()
+        h0 = time.perf_counter()
+        with torch.cuda.graph(graph, stream=stream):
+            for s in range(args.steps):
+                sl = slice(s * layers, (s + 1) * layers)
+                wb.step(stream, ev_score=(ev_s[0][sl], ev_s[1][sl]), ev_dec=(ev_d[0][sl], ev_d[1][sl]),
+                        graph=True, record=rec_ext)
+        host_ms = (time.perf_counter() - h0) * 1e3 / args.steps
+        launches = K.kvsel_launch_count() - launches0
+        graph.replay()                  # uploads the graph; untimed
+        stream.synchronize()
+        reset_state()
         clocks = ClockSampler(local)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         clocks.start()
-        launches0 = K.kvsel_launch_count()
         t0.record(stream)
-        for s in range(args.steps):
-            sl = slice(s * layers, (s + 1) * layers)
-            wb.step(stream, ev_score=(ev_s[0][sl], ev_s[1][sl]), ev_dec=(ev_d[0][sl], ev_d[1][sl]))
+        graph.replay()
         t1.record(stream)
         stream.synchronize()
-        launches = K.kvsel_launch_count() - launches0
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -289,10 +359,12 @@ def run_gpu(args):
             kv_dev = torch.empty_like(kv_host, device=device)
             out_dev = torch.empty((layers, w.batch, w.n_qheads, w.head_dim), dtype=torch.float32, device=device)
             out_host = torch.empty(out_dev.shape, dtype=torch.float32).pin_memory()
-            nks = [kv_dev[l, 0] for l in range(layers)]
-            nvs = [kv_dev[l, 1] for l in range(layers)]
-            qs = [q_dev[l] for l in range(layers)]
-            outs = [out_dev[l] for l in range(layers)]
+            import ctypes
+            vp = ctypes.c_void_p
+            nks = [vp(kv_dev[l, 0].data_ptr()) for l in range(layers)]
+            nvs = [vp(kv_dev[l, 1].data_ptr()) for l in range(layers)]
+            qs = [vp(q_dev[l].data_ptr()) for l in range(layers)]
+            outs = [vp(out_dev[l].data_ptr()) for l in range(layers)]
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
@@ -300,7 +372,7 @@ def run_gpu(args):
             for _ in range(n_e2e):
                 q_dev.copy_(q_host, non_blocking=True)
                 kv_dev.copy_(kv_host, non_blocking=True)
-                wb.step(stream, q_list=qs, out_list=outs, nk_list=nks, nv_list=nvs)
+                wb.step(stream, q_ptrs=qs, out_ptrs=outs, nk_ptrs=nks, nv_ptrs=nvs)
                 out_host.copy_(out_dev, non_blocking=True)
             e1.record(stream)
             stream.synchronize()
@@ -346,11 +418,14 @@ def run_gpu(args):
                               "achieved_gbs": dec_gbs, "frac": dec_gbs / peak},
         },
         "gpu_launches": int(launches),
+        "host_capture_ms_per_step": host_ms,
+        "timing": "one CUDA-graph replay of the timed steps (kernels launched through the C ABI "
+                  "during capture); per-launch durations from external event nodes",
         "clocks": clk,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_subprocess(args.ref_seqs, reps=3)
+        line["cpu_baseline"] = cpu_baseline_subprocess(args.ref_seqs, reps=5)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -411,7 +486,8 @@ def _oracle_worker(n_seqs, reps, out_path):
     k = w.k_for(w.keep[0])
     scale = 1.0 / math.sqrt(w.head_dim)
     times = []
-    for _ in range(reps):
+    t_start = time.perf_counter()
+    while len(times) < reps or time.perf_counter() - t_start < 10.0:
         t = time.perf_counter()
         oracle_step(w, seqs, k, scale, state)
         times.append(time.perf_counter() - t)
@@ -437,7 +513,8 @@ def cpu_baseline_subprocess(n_seqs: int, reps: int):
     layer_step_s = t * r["batch"] / r["n_seqs"]
     return {"value": 1.0 / layer_step_s, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"one layer, {n_seqs} of 16 sequences (append, score, Top-k, spans, "
-                      f"attention over 128 blocks); median of {reps}; scaled to a 16-sequence layer-step",
+                      f"attention over 128 blocks), repeated for >= 10 s ({len(r['times'])} reps); "
+                      f"median rep scaled to a 16-sequence layer-step",
             "seconds_per_sample": t}
 
 

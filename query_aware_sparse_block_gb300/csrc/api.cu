@@ -19,6 +19,10 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
+int g_smem_optin[kMaxDevices] = {};
+struct SmemEntry { int dev; const void* fn; int bytes; };
+SmemEntry g_smem_set[256];
+int g_smem_n = 0;
 std::atomic<uint64_t> g_launches{0};
 thread_local char g_msg[512] = "";
 
@@ -58,6 +62,35 @@ int sm_count() {
     g_sms[d] = n > 0 ? n : 1;
   }
   return g_sms[d];
+}
+
+int max_smem_optin() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_smem_optin[d]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+    g_smem_optin[d] = n;
+  }
+  return g_smem_optin[d];
+}
+
+cudaError_t ensure_smem(const void* kernel, int bytes) {
+  const int d = current_device();
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int i = 0; i < g_smem_n; ++i) {
+    SmemEntry& e = g_smem_set[i];
+    if (e.dev == d && e.fn == kernel) {
+      if (e.bytes >= bytes) return cudaSuccess;
+      const cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (r == cudaSuccess) e.bytes = bytes;
+      return r;
+    }
+  }
+  const cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (r == cudaSuccess && g_smem_n < 256) g_smem_set[g_smem_n++] = SmemEntry{d, kernel, bytes};
+  return r;
 }
 
 void count_launch(int n) { g_launches.fetch_add(uint64_t(n), std::memory_order_relaxed); }

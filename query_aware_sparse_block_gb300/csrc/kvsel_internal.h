@@ -15,6 +15,10 @@ namespace kvsel {
 int* device_error_word();
 void count_launch(int n = 1);
 int sm_count();
+int max_smem_optin();
+// Raises the kernel's dynamic shared-memory limit to at least `bytes`, calling
+// the runtime only the first time a larger size is needed on this device.
+cudaError_t ensure_smem(const void* kernel, int bytes);
 void set_last_error(const char* fmt, ...);
 
 // ---- summaries (summaries.cu) ----

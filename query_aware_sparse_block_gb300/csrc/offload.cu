@@ -107,8 +107,7 @@ cudaError_t launch_fetch_spans(const kvsel_problem& p, const kvsel_kv_src& kv,
   dim3 grid(per_seq, p.batch);
   const size_t smem = (size_t(p.k_max) + 1) * 4;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(fetch_spans_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    cudaError_t e = ensure_smem(reinterpret_cast<const void*>(fetch_spans_kernel), int(smem));
     if (e != cudaSuccess) return e;
   }
   fetch_spans_kernel<<<grid, kThreads, smem, s>>>(kv.host_kv, kv.staging, seq_lens, span_start,

@@ -33,10 +33,10 @@
 namespace kvsel {
 namespace {
 
-constexpr int kW = 4;                  // warps per CTA, each with its own tile ring
+constexpr int kW = 8;                  // consumer warps per CTA (16 token rows each per tile)
 constexpr int kThreads = kW * 32;
 constexpr int kMaxCtas = 512;          // partial-slot capacity of the workspace
-constexpr int kMinTilesPerCta = 2 * kW;
+constexpr int kMinTilesPerCta = 8;
 constexpr int kMaxStages = 8;
 
 struct DecodeArgs {
@@ -58,11 +58,12 @@ struct DecodeArgs {
   int* err;
   int batch, Hq, Hkv, G, B, max_blocks, k_max;
   int stages;
+  int kv_swap;   // 1: V precedes K in the tensor map (V tile lands first)
 };
 
 struct Tile {
   int b, j, h, cnt;
-  int rk, rv;
+  int rk;
   bool ok;
 };
 
@@ -113,12 +114,10 @@ __device__ Tile tile_info(const DecodeArgs& a, const int* base_s, const int* tle
     int64_t page = ok ? a.block_table[int64_t(b) * a.max_blocks + n] : 0;
     if (page < 0 || page >= a.n_pages) { ok = false; page = 0; }
     t.rk = int((page * a.Hkv + t.j) * a.B + t.h * BT);
-    t.rv = t.rk;
   } else {
     int64_t slot = o;
     if (slot >= a.slots) { ok = false; slot = 0; }
     t.rk = int((((int64_t(b) * a.slots + slot) * 2) * a.Hkv + t.j) * a.B + t.h * BT);
-    t.rv = t.rk + a.Hkv * a.B;
   }
   if (!ok && report) latch_error(a.err, KVSEL_ERR_BOUNDS);
   t.ok = ok;
@@ -136,31 +135,32 @@ __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int c) {
 
 template <int D, int BT>
 __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
-    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-    DecodeArgs a) {
+    const __grid_constant__ CUtensorMap tmKV, DecodeArgs a) {
   constexpr int kTileBytes = BT * D * 2;     // one of K or V
   constexpr int kStageBytes = 2 * kTileBytes;
-  constexpr int kBoxes = D / 64;
   constexpr int kKS = D / 16;                // k-steps of Q K^T
   constexpr int kNT = D / 8;                 // n-tiles of P V
+  constexpr int kWPR = BT / 16;              // warps sharing one tile ring (16 tokens each)
+  constexpr int kRings = kW / kWPR;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // carve: [stages][W] tiles (1024-aligned) | barriers | merge area | base | tlen
+  // carve: [stages][rings] tiles (1024-aligned) | barriers | merge area | base | tlen
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
   const int G = a.G;
   unsigned char* tiles = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + size_t(S) * kW * kStageBytes);
-  float* merge = reinterpret_cast<float*>(bars + S * kW);          // [W][G][D+2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + size_t(S) * kRings * kStageBytes);
+  float* merge = reinterpret_cast<float*>(bars + S * kRings);      // [W][G][D+2]
   int* base_s = reinterpret_cast<int*>(merge + kW * G * (D + 2));  // [batch+1]
   int* tlen_s = base_s + a.batch + 1;                              // [batch]
   __shared__ int flag_s;
+  __shared__ int scan_s[kW];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int ring = warp / kWPR, half = warp % kWPR;
   const int SUB = a.B / BT;
 
   // ---- per-sequence tile counts and prefix ----
-  __shared__ int scan_s[kW];
   int carry = 0;
   for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
     const int b = b0 + tid;
@@ -224,40 +224,71 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
   if (g0 >= g1) return;
 
   if (tid == 0) {
-    for (int i = 0; i < S * kW; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < S * kRings; ++i) mbar_init(&bars[i], 1);
     fence_barrier_init();
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
+    prefetch_tensormap(&tmKV);
   }
   __syncthreads();
 
-  // ---- this warp's tile stream ----
+  // ---- this ring's tile stream: tiles g0 + ring + m * kRings ----
   const int64_t L = g1 - g0;
-  const int count_w = L > warp ? int((L - warp + kW - 1) / kW) : 0;
+  const int count_r = L > ring ? int((L - ring + kRings - 1) / kRings) : 0;
   const uint32_t tiles_base = smem_u32(tiles);
-  auto slot_addr = [&](int m) -> uint32_t {
-    return tiles_base + uint32_t(((m % S) * kW + warp) * kStageBytes);
-  };
-  auto slot_bar = [&](int m) -> uint64_t* { return &bars[(m % S) * kW + warp]; };
-  int issued = 0;
-  bool dead = false;
-  auto issue = [&](int m) {
-    const Tile t = tile_info<BT>(a, base_s, tlen_s, g0 + warp + int64_t(m) * kW, true);
-    uint64_t* bar = slot_bar(m);
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    unsigned char* dst = tiles + ((m % S) * kW + warp) * kStageBytes;
-#pragma unroll
-    for (int x = 0; x < kBoxes; ++x) {
-      tma_load_2d(dst + x * BT * 128, &tmK, x * 64, t.rk, bar);
-      tma_load_2d(dst + kTileBytes + x * BT * 128, &tmV, x * 64, t.rv, bar);
+  auto slot_off = [&](int m) -> int { return ((m % S) * kRings + ring) * kStageBytes; };
+  auto slot_bar = [&](int m) -> uint64_t* { return &bars[(m % S) * kRings + ring]; };
+  const bool leader = (half == 0);
+  auto ring_sync = [&]() {
+    if constexpr (kWPR > 1) {
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + ring), "r"(kWPR * 32) : "memory");
+    } else {
+      __syncwarp();
     }
   };
-  if (lane == 0)
-    for (int m = 0; m < min(S, count_w); ++m) issue(m);
-  issued = min(S, count_w);
+  int issued = 0;
+  bool dead = false;
+  // Tile descriptors, 32 at a time: lane i holds the TMA rows and the valid
+  // token count of the ring's tile (cbase + i) in `cur` and of tile
+  // (cbase + 32 + i) in `nxt`. Their block-table and selection loads are
+  // issued a whole batch ahead, so no global load sits between a tile's
+  // consumption and the next copy.
+  int cbase = 0;
+  int cur_rk = 0, cur_cnt = 0, nxt_rk = 0, nxt_cnt = 0;
+  auto load_batch = [&](int base, int& rk, int& cnt) {
+    const int m = base + lane;
+    rk = cnt = 0;
+    if (m < count_r) {
+      const Tile t = tile_info<BT>(a, base_s, tlen_s, g0 + ring + int64_t(m) * kRings, leader);
+      rk = t.rk;
+      cnt = t.ok ? max(t.cnt, 0) : 0;
+    }
+  };
+  // all lanes: descriptor of ring tile m, with cbase <= m < cbase + 64
+  auto tile_desc = [&](int m, int& rk, int& cnt) {
+    const int i = m - cbase;
+    const int src = i & 31;
+    const int rk0 = __shfl_sync(0xffffffffu, cur_rk, src), rk1 = __shfl_sync(0xffffffffu, nxt_rk, src);
+    const int c0 = __shfl_sync(0xffffffffu, cur_cnt, src), c1 = __shfl_sync(0xffffffffu, nxt_cnt, src);
+    rk = i < 32 ? rk0 : rk1;
+    cnt = i < 32 ? c0 : c1;
+  };
+  // one 4-D box brings the K and V halves of a tile: [kv][half][row][64 channels]
+  auto issue = [&](int m, int rk) {   // ring leader, lane 0 only
+    uint64_t* bar = slot_bar(m);
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    tma_load_4d(tiles + slot_off(m), &tmKV, 0, rk, 0, 0, bar);
+  };
+  load_batch(0, cur_rk, cur_cnt);
+  load_batch(32, nxt_rk, nxt_cnt);
+  for (int m = 0; m < min(S, count_r); ++m) {
+    int rk, cnt;
+    tile_desc(m, rk, cnt);
+    if (leader && lane == 0) issue(m, rk);
+  }
+  issued = min(S, count_r);
   int m_cur = 0;
 
   const int gq = lane >> 2, tq = lane & 3;   // mma group / thread-in-group
+  const int r0 = half * 16;                  // this warp's 16 token rows of each tile
   int64_t g = g0;
   while (g < g1) {
     // ---- segment (b, j) containing g ----
@@ -288,109 +319,132 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
     float mrow[2] = {-INFINITY, -INFINITY};
     float lrow[2] = {0.f, 0.f};
 
-    while (m_cur < count_w && g0 + warp + int64_t(m_cur) * kW < sg1) {
-      const int64_t gt = g0 + warp + int64_t(m_cur) * kW;
-      const Tile t = tile_info<BT>(a, base_s, tlen_s, gt, false);
+    while (m_cur < count_r && g0 + ring + int64_t(m_cur) * kRings < sg1) {
+      if (m_cur == cbase + 32) {           // advance the descriptor window
+        cbase += 32;
+        cur_rk = nxt_rk; cur_cnt = nxt_cnt;
+        load_batch(cbase + 32, nxt_rk, nxt_cnt);
+      }
+      int t_rk, t_cnt;
+      tile_desc(m_cur, t_rk, t_cnt);
       if (!dead && !mbar_wait_bounded(slot_bar(m_cur), uint32_t((m_cur / S) & 1))) {
         dead = true;
         if (lane == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
       }
-      if (!dead && t.ok && t.cnt > 0) {
-        const uint32_t kt_base = slot_addr(m_cur);
-        const uint32_t vt_base = kt_base + kTileBytes;
-        if (t.cnt < BT) {
+      const int cnt = t_cnt - r0;            // valid tokens in this warp's 16 rows
+      if (!dead && cnt > 0) {
+        const int k_off = a.kv_swap ? kTileBytes : 0, v_off = a.kv_swap ? 0 : kTileBytes;
+        const uint32_t kt_base = tiles_base + slot_off(m_cur) + k_off;
+        const uint32_t vt_base = tiles_base + slot_off(m_cur) + v_off;
+        if (cnt < 16) {
           // rows past the sequence end: zero V so that 0 * garbage cannot poison P V
-          unsigned char* vt = tiles + ((m_cur % S) * kW + warp) * kStageBytes + kTileBytes;
-          for (int idx = lane; idx < (BT - t.cnt) * (D / 8); idx += 32) {
-            const int row = t.cnt + idx / (D / 8);
+          unsigned char* vt = tiles + slot_off(m_cur) + v_off;
+          for (int idx = lane; idx < (16 - cnt) * (D / 8); idx += 32) {
+            const int row = r0 + cnt + idx / (D / 8);
             const int c = (idx % (D / 8)) * 8;
-            const uint32_t off = swz<BT>(0, row, c);
-            *reinterpret_cast<uint4*>(vt + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vt + swz<BT>(0, row, c)) = make_uint4(0, 0, 0, 0);
           }
           __syncwarp();
         }
+        // S = Q K^T over 16 tokens: two n-tiles, even / odd k-steps in separate
+        // accumulators so that four independent mma chains are in flight
+        float sa[2][4], sb[2][4];
 #pragma unroll
-        for (int kt = 0; kt < BT / 16; ++kt) {
-          float s[2][4];
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-          {
-            const int row = kt * 16 + (lane & 7) + ((lane >> 4) << 3);
-            const int cofs = ((lane >> 3) & 1) * 8;
+          for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
+        {
+          const int row = r0 + (lane & 7) + ((lane >> 4) << 3);
+          const int cofs = ((lane >> 3) & 1) * 8;
 #pragma unroll
-            for (int ks = 0; ks < kKS; ++ks) {
-              uint32_t b0, b1, b2, b3;
-              ldsm_x4(swz<BT>(kt_base, row, ks * 16 + cofs), b0, b1, b2, b3);
-              mma_bf16_16816(s[0], qa[ks], b0, b1);
-              mma_bf16_16816(s[1], qa[ks], b2, b3);
+          for (int ks = 0; ks < kKS; ++ks) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(swz<BT>(kt_base, row, ks * 16 + cofs), b0, b1, b2, b3);
+            if (ks & 1) {
+              mma_bf16_16816(sb[0], qa[ks], b0, b1);
+              mma_bf16_16816(sb[1], qa[ks], b2, b3);
+            } else {
+              mma_bf16_16816(sa[0], qa[ks], b0, b1);
+              mma_bf16_16816(sa[1], qa[ks], b2, b3);
             }
           }
-          // scale, mask, online softmax (rows gq and gq + 8)
-          float mx[2] = {-INFINITY, -INFINITY};
+        }
+        float s[2][4];
+        float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tok = kt * 16 + nt * 8 + 2 * tq + (e & 1);
-              const float x = tok < t.cnt ? s[nt][e] * a.scale_log2 : -INFINITY;
-              s[nt][e] = x;
-              mx[e >> 1] = fmaxf(mx[e >> 1], x);
-            }
-          float alpha[2], mu[2];
+          for (int e = 0; e < 4; ++e) {
+            const int tok = nt * 8 + 2 * tq + (e & 1);
+            const float x = tok < cnt ? (sa[nt][e] + sb[nt][e]) * a.scale_log2 : -INFINITY;
+            s[nt][e] = x;
+            mx[e >> 1] = fmaxf(mx[e >> 1], x);
+          }
+        float mu[2];
+        bool grow = false;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+          grow |= mx[r] > mrow[r];
+        }
+        if (__any_sync(0xffffffffu, grow)) {
+          // a running max moved: rescale the accumulators of every row
+          float alpha[2];
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-            mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
             const float mn = fmaxf(mrow[r], mx[r]);
-            mu[r] = (mn == -INFINITY) ? 0.f : mn;
-            alpha[r] = ex2(mrow[r] - mu[r]);
+            const float m_use = (mn == -INFINITY) ? 0.f : mn;
+            alpha[r] = ex2(mrow[r] - m_use);
             mrow[r] = mn;
+            lrow[r] *= alpha[r];
           }
-          float psum[2] = {0.f, 0.f};
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float p = ex2(s[nt][e] - mu[e >> 1]);
-              s[nt][e] = p;
-              psum[e >> 1] += p;
-            }
-#pragma unroll
-          for (int r = 0; r < 2; ++r) lrow[r] = lrow[r] * alpha[r] + psum[r];
 #pragma unroll
           for (int nt = 0; nt < kNT; ++nt) {
             o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
             o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
           }
-          uint32_t ph[4], pl[4];
+        }
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float x0 = s[i >> 1][(i & 1) * 2 + 0];
-            const float x1 = s[i >> 1][(i & 1) * 2 + 1];
-            ph[i] = pack_bf16x2(x0, x1);
-            pl[i] = pack_bf16x2(x0 - bf16lo(ph[i]), x1 - bf16hi(ph[i]));
+        for (int r = 0; r < 2; ++r) mu[r] = (mrow[r] == -INFINITY) ? 0.f : mrow[r];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float p = ex2(s[nt][e] - mu[e >> 1]);
+            s[nt][e] = p;
+            lrow[e >> 1] += p;
           }
-          {
-            const int row = kt * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int cofs = (lane >> 4) * 8;
+        uint32_t ph[4], pl[4];
 #pragma unroll
-            for (int dc = 0; dc < D / 16; ++dc) {
-              uint32_t v0, v1, v2, v3;
-              ldsm_x4_t(swz<BT>(vt_base, row, dc * 16 + cofs), v0, v1, v2, v3);
-              mma_bf16_16816(o[2 * dc], ph, v0, v1);
-              mma_bf16_16816(o[2 * dc], pl, v0, v1);
-              mma_bf16_16816(o[2 * dc + 1], ph, v2, v3);
-              mma_bf16_16816(o[2 * dc + 1], pl, v2, v3);
-            }
+        for (int i = 0; i < 4; ++i) {
+          const float x0 = s[i >> 1][(i & 1) * 2 + 0];
+          const float x1 = s[i >> 1][(i & 1) * 2 + 1];
+          ph[i] = pack_bf16x2(x0, x1);
+          pl[i] = pack_bf16x2(x0 - bf16lo(ph[i]), x1 - bf16hi(ph[i]));
+        }
+        {
+          const int row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+          const int cofs = (lane >> 4) * 8;
+#pragma unroll
+          for (int dc = 0; dc < D / 16; ++dc) {
+            uint32_t v0, v1, v2, v3;
+            ldsm_x4_t(swz<BT>(vt_base, row, dc * 16 + cofs), v0, v1, v2, v3);
+            mma_bf16_16816(o[2 * dc], ph, v0, v1);
+            mma_bf16_16816(o[2 * dc + 1], ph, v2, v3);
+            mma_bf16_16816(o[2 * dc], pl, v0, v1);
+            mma_bf16_16816(o[2 * dc + 1], pl, v2, v3);
           }
         }
       }
-      // release the slot and refill it S tiles ahead
-      __syncwarp();
-      if (!dead && m_cur + S < count_w) {
-        if (lane == 0) {
+      // release the slot (both warps of the ring are done) and refill it S tiles ahead
+      ring_sync();
+      if (!dead && m_cur + S < count_r) {
+        int rk, cnt2;
+        tile_desc(m_cur + S, rk, cnt2);
+        if (leader && lane == 0) {
           fence_proxy_async();
-          issue(m_cur + S);
+          issue(m_cur + S, rk);
         }
         issued = m_cur + S + 1;
       }
@@ -504,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
   }
 
   // drain copies still in flight (only after a timeout)
-  if (dead && lane == 0)
+  if (dead && leader && lane == 0)
     for (int m = m_cur; m < issued; ++m) (void)mbar_wait_bounded(slot_bar(m), uint32_t((m / S) & 1));
 }
 
@@ -522,40 +576,76 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int D, int BT) {
+// Tensor map over K and V together: dims (innermost first) are 64 channels,
+// cache rows (stride D*2 bytes), the D/64 channel halves (stride 128 bytes)
+// and K vs V (stride = distance between the two buffers). A box of
+// {64, BT, D/64, 2} with the 128-byte swizzle lands as [kv][half][row][64] in
+// shared memory, every 128-byte row swizzled by its row index.
+bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t kv_stride, int D, int BT) {
   auto enc = get_encode();
   if (!enc) return false;
-  cuuint64_t dims[2] = {cuuint64_t(D), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(D) * 2};
-  cuuint32_t box[2] = {64u, cuuint32_t(BT)};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  cuuint64_t dims[4] = {64u, cuuint64_t(rows), cuuint64_t(D / 64), 2u};
+  cuuint64_t strides[3] = {cuuint64_t(D) * 2, 128u, cuuint64_t(kv_stride)};
+  cuuint32_t box[4] = {64u, cuuint32_t(BT), cuuint32_t(D / 64), 2u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+// A tensor map depends only on (address, rows, K/V distance, D, BT): cache the
+// encodings so that a decode loop over the same buffers does no host-side
+// encoding.
+struct MapEntry {
+  const void* base;
+  int64_t rows, kv_stride;
+  int D, BT;
+  CUtensorMap map;
+};
+std::mutex g_map_mu;
+MapEntry g_maps[64];
+int g_map_next = 0, g_map_n = 0;
+
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t kv_stride, int D, int BT) {
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < g_map_n; ++i) {
+      const MapEntry& e = g_maps[i];
+      if (e.base == base && e.rows == rows && e.kv_stride == kv_stride && e.D == D && e.BT == BT) {
+        *m = e.map;
+        return true;
+      }
+    }
+  }
+  if (!encode_map(m, base, rows, kv_stride, D, BT)) return false;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  MapEntry& e = g_maps[g_map_next];
+  e.base = base; e.rows = rows; e.kv_stride = kv_stride; e.D = D; e.BT = BT; e.map = *m;
+  g_map_next = (g_map_next + 1) % 64;
+  if (g_map_n < 64) ++g_map_n;
+  return true;
+}
+
 template <int D, int BT>
-cudaError_t launch_t(const kvsel_problem& p, const DecodeArgs& a0, const CUtensorMap& mk,
-                     const CUtensorMap& mv, cudaStream_t s) {
+cudaError_t launch_t(const kvsel_problem& p, const DecodeArgs& a0, const CUtensorMap& mkv,
+                     cudaStream_t s) {
   DecodeArgs a = a0;
-  constexpr int kStageBytes = 2 * BT * D * 2;
+  constexpr int kRings = kW / (BT / 16);
+  constexpr int kGroupBytes = kRings * 2 * BT * D * 2;   // one stage of every ring
   // 1024: manual alignment of the tile area; 256: static shared variables
   const size_t rest = 1024 + 256 + size_t(kW) * a.G * (D + 2) * 4 + (size_t(p.batch) * 2 + 1) * 4;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int max_optin = 0;
-  cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  int stages = int((size_t(max_optin) - rest - 8 * kW * kMaxStages) / (size_t(kW) * kStageBytes));
+  const int max_optin = max_smem_optin();
+  int stages = int((size_t(max_optin) - rest - 8 * kRings * kMaxStages) / size_t(kGroupBytes));
   stages = std::min(kMaxStages, stages);
   if (stages < 1) return cudaErrorInvalidConfiguration;
   a.stages = stages;
-  const size_t smem = rest + size_t(stages) * kW * kStageBytes + 8 * kW * stages;
+  const size_t smem = rest + size_t(stages) * kGroupBytes + 8 * kRings * stages;
   auto kfn = sparse_decode_kernel<D, BT>;
-  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kfn), int(smem));
   if (e != cudaSuccess) return e;
   const int grid = std::min(kMaxCtas, sm_count());
-  kfn<<<grid, kThreads, smem, s>>>(mk, mv, a);
+  kfn<<<grid, kThreads, smem, s>>>(mkv, a);
   count_launch();
   return cudaGetLastError();
 }
@@ -591,20 +681,26 @@ cudaError_t launch_sparse_decode(const kvsel_problem& p, const kvsel_bf16* q,
   a.B = p.block_size; a.max_blocks = p.max_blocks; a.k_max = p.k_max;
   const int D = p.head_dim;
   const int BT = std::min(p.block_size, 32);
-  CUtensorMap mk, mv;
+  CUtensorMap mkv;
   if (a.kind == KVSEL_KV_PAGED) {
     const int64_t rows = kv.n_pages * p.n_kvheads * p.block_size;
-    if (!make_map(&mk, kv.k_pages, rows, D, BT) || !make_map(&mv, kv.v_pages, rows, D, BT))
+    const char* kb = reinterpret_cast<const char*>(kv.k_pages);
+    const char* vb = reinterpret_cast<const char*>(kv.v_pages);
+    const int64_t dist = vb > kb ? int64_t(vb - kb) : int64_t(kb - vb);
+    a.kv_swap = vb < kb ? 1 : 0;
+    if (dist == 0 || (dist & 15) || dist >= (int64_t(1) << 40)) return cudaErrorInvalidValue;
+    if (!make_map(&mkv, a.kv_swap ? kv.v_pages : kv.k_pages, rows, dist, D, BT))
       return cudaErrorInvalidValue;
   } else {
     const int64_t rows = int64_t(p.batch) * kv.staging_slots * 2 * p.n_kvheads * p.block_size;
-    if (!make_map(&mk, kv.staging, rows, D, BT)) return cudaErrorInvalidValue;
-    mv = mk;
+    const int64_t dist = int64_t(p.n_kvheads) * p.block_size * D * 2;
+    a.kv_swap = 0;
+    if (!make_map(&mkv, kv.staging, rows, dist, D, BT)) return cudaErrorInvalidValue;
   }
-  if (D == 128 && BT == 32) return launch_t<128, 32>(p, a, mk, mv, s);
-  if (D == 128 && BT == 16) return launch_t<128, 16>(p, a, mk, mv, s);
-  if (D == 64 && BT == 32) return launch_t<64, 32>(p, a, mk, mv, s);
-  if (D == 64 && BT == 16) return launch_t<64, 16>(p, a, mk, mv, s);
+  if (D == 128 && BT == 32) return launch_t<128, 32>(p, a, mkv, s);
+  if (D == 128 && BT == 16) return launch_t<128, 16>(p, a, mkv, s);
+  if (D == 64 && BT == 32) return launch_t<64, 32>(p, a, mkv, s);
+  if (D == 64 && BT == 16) return launch_t<64, 16>(p, a, mkv, s);
   return cudaErrorInvalidValue;
 }
 

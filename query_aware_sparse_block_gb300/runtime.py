@@ -75,3 +75,64 @@ class SparseDecoder:
                               dense_flag=self.dense_flag if use_dense_flag else None,
                               span_start=self.span_start, span_len=self.span_len,
                               n_spans=self.n_spans, out_bf16=out_bf16, stream=stream)
+
+
+class BoundLayer:
+    """Pre-marshalled C-ABI calls for one layer's fixed buffers.
+
+    A decode loop calls the same three entry points with the same buffers on
+    every step; only the step's position / length arrays and the stream
+    change. Converting every argument once keeps the host-side cost of a call
+    to a few microseconds, so the host enqueues ahead of the GPU.
+    """
+
+    def __init__(self, dec: SparseDecoder, q, k_pages, v_pages, block_table, summaries, open_acc,
+                 out, lse, kv=None, gamma=2.0, tau_rel=0.0, new_k=None, new_v=None):
+        L = K.lib()
+        vp = ctypes.c_void_p
+        self._fa, self._fs, self._fd = L.kvsel_build_summaries, L.kvsel_score_topk, L.kvsel_sparse_decode
+        self.dec = dec
+        self.p = ctypes.byref(dec.p)
+        self.kv = kv if kv is not None else K.kv_paged(k_pages, v_pages, block_table)
+        self.kv_ref = ctypes.byref(self.kv)
+        self.k_pages, self.v_pages = vp(k_pages.data_ptr()), vp(v_pages.data_ptr())
+        self.n_pages = int(k_pages.shape[0])
+        self.block_table = vp(block_table.data_ptr())
+        self.q = vp(q.data_ptr())
+        self.summ, self.acc = vp(summaries.data_ptr()), vp(open_acc.data_ptr())
+        self.new_k = vp(new_k.data_ptr()) if new_k is not None else None
+        self.new_v = vp(new_v.data_ptr()) if new_v is not None else None
+        self.out, self.lse = vp(out.data_ptr()), vp(lse.data_ptr())
+        self.gamma, self.tau = ctypes.c_float(gamma), ctypes.c_float(tau_rel)
+        d = dec
+        self.sel = (vp(d.sel_idx.data_ptr()), vp(d.n_sel.data_ptr()), vp(d.span_start.data_ptr()),
+                    vp(d.span_len.data_ptr()), vp(d.n_spans.data_ptr()), vp(d.dense_flag.data_ptr()))
+        self.kps = vp(d.k_per_seq.data_ptr())
+        self.ws1, self.ws1n = vp(d.ws_score.data_ptr()), ctypes.c_size_t(d.ws_score.numel())
+        self.ws2, self.ws2n = vp(d.ws_decode.data_ptr()), ctypes.c_size_t(d.ws_decode.numel())
+        self.scale = ctypes.c_float(d.scale)
+
+    def append(self, append_pos_ptr, stream_ptr, new_k_ptr=None, new_v_ptr=None):
+        nk = new_k_ptr if new_k_ptr is not None else self.new_k
+        nv = new_v_ptr if new_v_ptr is not None else self.new_v
+        rc = self._fa(self.p, K.KVSEL_SUMMARY_APPEND, self.k_pages, self.v_pages, self.n_pages,
+                      self.block_table, None, append_pos_ptr, nk, nv, self.summ, self.acc, stream_ptr)
+        if rc:
+            K._check(rc, "kvsel_build_summaries")
+
+    def select(self, seq_lens_ptr, stream_ptr, q_ptr=None):
+        s = self.sel
+        rc = self._fs(self.p, q_ptr if q_ptr is not None else self.q, self.summ, seq_lens_ptr,
+                      self.kps, self.gamma, self.tau, s[0], s[1], s[2], s[3], s[4], s[5], None,
+                      self.ws1, self.ws1n, stream_ptr)
+        if rc:
+            K._check(rc, "kvsel_score_topk")
+
+    def attend(self, seq_lens_ptr, stream_ptr, q_ptr=None, out_ptr=None):
+        s = self.sel
+        rc = self._fd(self.p, q_ptr if q_ptr is not None else self.q, self.kv_ref, seq_lens_ptr,
+                      s[0], s[1], s[2], s[3], s[4], s[5], self.scale,
+                      out_ptr if out_ptr is not None else self.out, None, self.lse,
+                      self.ws2, self.ws2n, stream_ptr)
+        if rc:
+            K._check(rc, "kvsel_sparse_decode")
