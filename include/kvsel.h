@@ -168,6 +168,36 @@ KVSEL_API int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, 
                       int32_t* span_start, int32_t* span_len, int32_t* n_spans,
                       kvsel_stream_t stream);
 
+/*
+ * kvsel_score_topk_noalloc -- kvsel_score_topk without a caller workspace.
+ * The pages describe no such entry point; it exists for callers that cannot
+ * allocate device memory: code embedded in a host framework that owns the
+ * whole device-memory budget and forbids allocations outside its own
+ * allocator, or a latency-critical path where the implicit synchronisation
+ * of cudaMalloc/cudaFree is not acceptable.
+ *
+ * Same arguments, results and errors as kvsel_score_topk minus ws/ws_bytes.
+ * Its scratch is a file-scope device array of kvsel_noalloc_scratch_bytes()
+ * bytes (4 MiB) that every GPU which loads the library holds until the
+ * process exits. A problem whose kvsel_workspace_size(p, KVSEL_WS_SCORE_TOPK)
+ * exceeds it (roughly batch * max_blocks > 1M) is rejected with
+ * KVSEL_ERR_WORKSPACE and nothing is enqueued. The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture. Each call clears
+ * the per-sequence tickets on `stream` before the kernel; no call allocates.
+ * All calls on a device share the one array, so calls that can overlap on
+ * the GPU (different streams without ordering between them) race.
+ */
+KVSEL_API int kvsel_score_topk_noalloc(const kvsel_problem* p, const kvsel_bf16* q,
+                                       const kvsel_bf16* summaries, const int32_t* seq_lens,
+                                       const int32_t* k_per_seq, float gamma, float tau_rel,
+                                       int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                                       int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                                       float* scores_out, kvsel_stream_t stream);
+
+/* Bytes of the static scratch array behind kvsel_score_topk_noalloc. */
+KVSEL_API size_t kvsel_noalloc_scratch_bytes(void);
+
 enum kvsel_kv_kind {
   KVSEL_KV_PAGED = 0,  /* K/V pages in device memory + block table */
   KVSEL_KV_STAGED = 1, /* selected blocks already in a device staging buffer */

@@ -79,6 +79,9 @@ _SIGS = {
                                    _P, _P, _P, _P, _P, _P]),
     "kvsel_score_topk": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, ctypes.c_float,
                               ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "kvsel_score_topk_noalloc": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, ctypes.c_float,
+                                      ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "kvsel_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "kvsel_merge_spans": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, _P, _P]),
     "kvsel_sparse_decode": (_I, [ctypes.POINTER(kvsel_problem), _P, ctypes.POINTER(kvsel_kv_src), _P,
                                  _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
@@ -217,6 +220,25 @@ def kvsel_score_topk(p, q, summaries, seq_lens, k_per_seq, sel_idx, n_sel, span_
                                   _ptr(dense_flag), _ptr(scores_out), _ptr(ws),
                                   ws.numel() * ws.element_size(), _stream(stream)),
            "kvsel_score_topk")
+
+
+def kvsel_score_topk_noalloc(p, q, summaries, seq_lens, k_per_seq, sel_idx, n_sel, span_start,
+                             span_len, n_spans, gamma=2.0, tau_rel=0.0, dense_flag=None,
+                             scores_out=None, stream=None):
+    """kvsel_score_topk with the library's static scratch instead of a workspace."""
+    for t, dt, n in ((q, torch.bfloat16, "q"), (summaries, torch.bfloat16, "summaries"),
+                     (seq_lens, torch.int32, "seq_lens"), (k_per_seq, torch.int32, "k_per_seq"),
+                     (sel_idx, torch.int32, "sel_idx"), (n_sel, torch.int32, "n_sel"),
+                     (span_start, torch.int32, "span_start"), (span_len, torch.int32, "span_len"),
+                     (n_spans, torch.int32, "n_spans"), (dense_flag, torch.uint8, "dense_flag"),
+                     (scores_out, torch.float32, "scores_out")):
+        _expect(t, dt, n)
+    _check(lib().kvsel_score_topk_noalloc(ctypes.byref(p), _ptr(q), _ptr(summaries), _ptr(seq_lens),
+                                          _ptr(k_per_seq), float(gamma), float(tau_rel),
+                                          _ptr(sel_idx), _ptr(n_sel), _ptr(span_start),
+                                          _ptr(span_len), _ptr(n_spans), _ptr(dense_flag),
+                                          _ptr(scores_out), _stream(stream)),
+           "kvsel_score_topk_noalloc")
 
 
 def kvsel_merge_spans(p, sel_idx, n_sel, span_start, span_len, n_spans, stream=None):
