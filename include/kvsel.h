@@ -34,20 +34,28 @@
  *
  * Layouts (row-major, innermost last)
  *  q            [batch][n_qheads][head_dim]                    bf16
- *  K / V pages  [n_pages][n_kvheads][block_size][head_dim]     bf16
+ *  K / V pages  [n_pages][n_kvheads][head_dim/64][block_size][64] bf16,
+ *               "tiled": each (page, KV head) tile keeps its block_size x
+ *               head_dim keys as head_dim/64 column halves of block_size rows
+ *               x 64 channels, and inside every 128-byte row the 16-byte chunk
+ *               c of token row t is stored at chunk position c ^ (t % 8). A
+ *               tile is therefore one contiguous range, and so is a run of
+ *               consecutive heads of a page.
  *  block_table  [batch][max_blocks]                            int32 (page id)
  *  seq_lens     [batch]                                        int32 (T_b)
  *  summaries    [batch][max_blocks][n_kvheads][head_dim]       bf16
  *  open_acc     [batch][n_kvheads][head_dim]                   fp64
  *  sel_idx      [batch][k_max]  ascending block indices        int32
  *  spans        span_start / span_len [batch][k_max]           int32
- *  host tier    [batch][host_blocks][2][n_kvheads][block_size][head_dim] bf16
- *               (K then V of one block contiguous, spans contiguous)
- *  staging      [batch][staging_slots][2][n_kvheads][block_size][head_dim] bf16
+ *  host tier    [batch][host_blocks][2][one page of K or V] bf16, tiled as the
+ *               pages (K then V of one block contiguous, spans contiguous)
+ *  staging      [batch][staging_slots][2][one page of K or V] bf16, tiled
  *  out          [batch][n_qheads][head_dim] fp32; lse [batch][n_qheads] fp32
  * A sequence b holds T_b = seq_lens[b] tokens in N_b = ceil(T_b / block_size)
  * blocks; token t lives in page block_table[b][t / block_size], row
- * t % block_size.
+ * t % block_size. Channel c of token row t of KV head j of page p is element
+ * ((p * n_kvheads + j) * head_dim/64 + c/64) * block_size * 64 + t * 64 +
+ * (((c % 64) / 8) ^ (t % 8)) * 8 + c % 8.
  */
 #ifndef KVSEL_H_
 #define KVSEL_H_
@@ -116,7 +124,8 @@ enum kvsel_summary_mode {
  *
  * k_pages, v_pages: paged cache (v_pages only written by APPEND with new_v).
  * block_table, seq_lens: device int32. append_pos: device [batch] int32.
- * new_k, new_v: device [batch][n_kvheads][head_dim] bf16, nullable.
+ * new_k, new_v: device [batch][n_kvheads][head_dim] bf16 in natural channel
+ * order, nullable; they are stored into the tiled page layout.
  * summaries: device output. open_acc: device [batch][n_kvheads][head_dim] fp64.
  * Errors: INVALID_ARG (null required pointer, bad shape), UNSUPPORTED, CUDA;
  * device BOUNDS when a block-table entry is negative or >= n_pages or

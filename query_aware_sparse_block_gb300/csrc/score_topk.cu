@@ -63,15 +63,6 @@ __device__ __forceinline__ uint32_t order_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(smem_dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Block-wide exclusive scan of one int per thread; returns the prefix and the
 // block total through *total. scratch: kWarps ints.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {

@@ -5,41 +5,62 @@
 // flash-style log-sum-exp reduction of the DKV abstract.
 //
 // Design (GB300):
-//  * Work list: for every sequence b and KV head j, the attended blocks of b
-//    are cut into sub-tiles of BT = min(B, 32) tokens; the flattened list of
-//    (b, j, block, half) sub-tiles is split into equal contiguous ranges, one
-//    per CTA (one CTA per SM), so the HBM stream is balanced whatever the
-//    per-sequence selection sizes are (stream-K style). A (b, j) segment that
-//    a CTA owns entirely is finished in place; a segment cut between CTAs is
-//    finished by the last contributor (an atomic ticket, no waiting).
-//  * Movement: each K or V sub-tile is one or two 2-D TMA boxes (64 channels x
-//    BT rows, 128-byte swizzle) landing in shared memory; each of the four
-//    warps owns a ring of stages and issues its own copies S tiles ahead, so
-//    up to 4*S tiles per SM are in flight.
+//  * Work unit: a tile is one attended block of one sequence for a group of
+//    HPG consecutive KV heads. The selection is per sequence, so all heads of
+//    a page are needed, and a page stores its heads contiguously in the tiled
+//    layout: the tile's K is one contiguous range, its V another. Two 1-D bulk
+//    (TMA) copies move them into shared memory unchanged; HPG is chosen so
+//    that each is 16 KiB for d = 128, which keeps DRAM bursts long (scattered
+//    bulk copies of >= 16 KiB stream near the HBM read peak, tensor-map boxes
+//    of 128-byte rows do not). The tiled layout already carries the 16-byte chunk swizzle
+//    (chunk c of row t at c ^ (t % 8)), so ldmatrix reads are conflict-free.
+//  * Work list: the flattened (sequence, head group, block) tiles are split
+//    into equal contiguous ranges, one per CTA (one CTA per SM), so the HBM
+//    stream is balanced whatever the per-sequence selection sizes are. At the
+//    end of each (sequence, head group) segment every warp stores its online-
+//    softmax state (max, sum, unnormalised output) to global memory and moves
+//    on without any synchronisation; a second small kernel, launched as a
+//    programmatic dependent of the first so that it is already resident,
+//    merges the states of each output row by log-sum-exp.
+//  * Pipeline: two rings of 4 warps; ring r takes every other tile of the
+//    CTA's range and keeps S of them in flight. Each warp of a ring owns one
+//    (head, 16-token slice) of its ring's tiles; the last warp to finish a
+//    slot (a shared-memory counter) refills it, so no warp waits on another
+//    and the two rings drift apart instead of hitting the tensor pipe in
+//    lockstep.
 //  * Math: the GQA group's query heads (G <= 16, zero-padded to 16 rows) form
 //    the A operand of mma.m16n8k16 bf16 tensor-core tiles: S = Q K^T with K
 //    read by ldmatrix from the swizzled tile, online softmax in fp32 (exp2 of
-//    log2-scaled logits), then O += P V with V read by ldmatrix.trans; P is
-//    split into bf16 high and low parts so the product keeps ~16 bits.
+//    log2-scaled logits, accumulators rescaled only when a row max moves),
+//    then O += P V with V read by ldmatrix.trans; P is split into bf16 high
+//    and low parts so the product keeps ~16 bits.
 //  * Every wait on a copy is bounded; a wait that runs out latches
 //    KVSEL_ERR_TIMEOUT and the warp stops issuing work.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "kvsel_common.cuh"
 #include "kvsel_internal.h"
 
 namespace kvsel {
 namespace {
 
-constexpr int kW = 8;                  // consumer warps per CTA (16 token rows each per tile)
+constexpr int kW = 8;                  // warps per CTA
+constexpr int kRingWarps = 4;          // warps sharing one tile ring: one (head, 16-token slice) each
+constexpr int kRings = kW / kRingWarps;
 constexpr int kThreads = kW * 32;
 constexpr int kMaxCtas = 512;          // partial-slot capacity of the workspace
-constexpr int kMinTilesPerCta = 8;
+constexpr int kMinTilesPerCta = 4;
 constexpr int kMaxStages = 8;
 
+// Heads per tile for block size B and H_kv heads: as many as keep the tile
+// at 64 token rows (4 warps x 16 rows), and a divisor of H_kv.
+inline int heads_per_group(int B, int Hkv) {
+  int h = std::min(Hkv, kRingWarps * 16 / B);
+  while (h > 1 && Hkv % h) --h;
+  return std::max(1, h);
+}
+
 struct DecodeArgs {
+  const kvsel_bf16* k_base;   // PAGED: K pages; STAGED: staging
+  const kvsel_bf16* v_base;   // PAGED: V pages
   const kvsel_bf16* q;
   const int32_t* seq_lens;
   const int32_t* sel_idx;
@@ -53,18 +74,12 @@ struct DecodeArgs {
   float* out;
   kvsel_bf16* out_bf16;
   float* lse;
-  float* partials;
-  uint32_t* tickets;
+  float* partials;     // warp states: [(cta + segment) * W + warp][G][D + 2]
+  int* meta;           // [0] total tiles, [1] active CTAs, [2 ..] tile prefix per sequence
   int* err;
   int batch, Hq, Hkv, G, B, max_blocks, k_max;
+  int hpg, n_groups;   // heads per tile, head groups per sequence
   int stages;
-  int kv_swap;   // 1: V precedes K in the tensor map (V tile lands first)
-};
-
-struct Tile {
-  int b, j, h, cnt;
-  int rk;
-  bool ok;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -87,78 +102,77 @@ __device__ __forceinline__ int find_seq(const int* base_s, int batch, int64_t g)
   return lo;
 }
 
-template <int BT>
-__device__ __forceinline__ int sub_per_block(int B) { return B / BT; }
-
-template <int BT>
-__device__ Tile tile_info(const DecodeArgs& a, const int* base_s, const int* tlen_s, int64_t g,
-                          bool report) {
-  Tile t;
-  const int SUB = sub_per_block<BT>(a.B);
+// Copy unit of tile g (the K head-group tile's index in units of HPG*B*d
+// elements) and its valid token count (0 when the tile is skipped).
+__device__ void tile_info(const DecodeArgs& a, const int* base_s, const int* tlen_s, int64_t g,
+                          bool report, int& unit, int& cnt) {
   const int b = find_seq(base_s, a.batch, g);
   const int64_t r = g - base_s[b];
-  const int nb = (base_s[b + 1] - base_s[b]) / (a.Hkv * SUB);
-  const int seg = nb * SUB;
-  t.b = b;
-  t.j = int(r / seg);
-  const int rr = int(r % seg);
-  const int o = rr / SUB;
-  t.h = rr % SUB;
+  const int nb = (base_s[b + 1] - base_s[b]) / a.n_groups;
+  const int hg = int(r / nb);
+  const int o = int(r % nb);
   const int T = tlen_s[b];
   const int N = (T + a.B - 1) / a.B;
   const bool dense = a.dense_flag && a.dense_flag[b];
   const int n = dense ? o : a.sel_idx[int64_t(b) * a.k_max + o];
   bool ok = (n >= 0 && n < N);
-  t.cnt = ok ? min(BT, T - n * a.B - t.h * BT) : 0;
+  cnt = ok ? min(a.B, T - n * a.B) : 0;
   if (a.kind == KVSEL_KV_PAGED) {
     int64_t page = ok ? a.block_table[int64_t(b) * a.max_blocks + n] : 0;
     if (page < 0 || page >= a.n_pages) { ok = false; page = 0; }
-    t.rk = int((page * a.Hkv + t.j) * a.B + t.h * BT);
+    unit = int(page * a.n_groups + hg);
   } else {
     int64_t slot = o;
     if (slot >= a.slots) { ok = false; slot = 0; }
-    t.rk = int((((int64_t(b) * a.slots + slot) * 2) * a.Hkv + t.j) * a.B + t.h * BT);
+    unit = int((int64_t(b) * a.slots + slot) * 2 * a.n_groups + hg);
   }
-  if (!ok && report) latch_error(a.err, KVSEL_ERR_BOUNDS);
-  t.ok = ok;
-  return t;
+  if (!ok) {
+    cnt = 0;
+    if (report) latch_error(a.err, KVSEL_ERR_BOUNDS);
+  }
 }
 
-// Swizzled shared address of (row, channel c, c % 8 == 0) in a tile made of
-// 64-channel TMA boxes with the 128-byte swizzle (16-byte chunk ^= row % 8).
-template <int BT>
-__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int c) {
-  const int box = c >> 6;
+// Shared address of (plane, head h of the group, token row, channel c with
+// c % 8 == 0) in a stage holding the tiled K and V head-group tiles:
+// [plane][head][d/64][row][64], 16-byte chunk c of row t at c ^ (t % 8).
+__device__ __forceinline__ uint32_t swz(uint32_t stage, int plane_bytes, int plane, int h,
+                                        int halves, int B, int row, int c) {
+  const int half = c >> 6;
   const int chunk = (c & 63) >> 3;
-  return tile + box * (BT * 128) + row * 128 + ((chunk ^ (row & 7)) << 4);
+  return stage + uint32_t(plane * plane_bytes) +
+         uint32_t(((h * halves + half) * B + row) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D, int BT>
-__global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
-    const __grid_constant__ CUtensorMap tmKV, DecodeArgs a) {
-  constexpr int kTileBytes = BT * D * 2;     // one of K or V
-  constexpr int kStageBytes = 2 * kTileBytes;
-  constexpr int kKS = D / 16;                // k-steps of Q K^T
-  constexpr int kNT = D / 8;                 // n-tiles of P V
-  constexpr int kWPR = BT / 16;              // warps sharing one tile ring (16 tokens each)
-  constexpr int kRings = kW / kWPR;
+template <int D, int B, int NTH>
+__global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a) {
+  constexpr int kWPH = B / 16;               // warps (16-token slices) per head
+  constexpr int kMT = D / 16;                // 16-channel m-tiles of O^T
+  static_assert(kWPH <= kRingWarps, "block larger than a ring");
+  constexpr int kKS = D / 16;                // k-steps of K Q^T
+  constexpr int kHalves = D / 64;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // carve: [stages][rings] tiles (1024-aligned) | barriers | merge area | base | tlen
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = a.stages;
   const int G = a.G;
+  const int HPG = a.hpg;
+  const int plane_elems = HPG * B * D;      // one head-group tile of K (or V)
+  const int plane_bytes = plane_elems * 2;
+  const int tile_bytes = 2 * plane_bytes;    // K + V
   unsigned char* tiles = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + size_t(S) * kRings * kStageBytes);
-  float* merge = reinterpret_cast<float*>(bars + S * kRings);      // [W][G][D+2]
-  int* base_s = reinterpret_cast<int*>(merge + kW * G * (D + 2));  // [batch+1]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tiles + size_t(S) * kRings * tile_bytes);
+  int* done_s = reinterpret_cast<int*>(bars + S * kRings);          // [S][rings] consumer counts
+  int* base_s = done_s + 2 * kMaxStages * kRings;                  // [batch+1]
   int* tlen_s = base_s + a.batch + 1;                              // [batch]
-  __shared__ int flag_s;
   __shared__ int scan_s[kW];
 
+  // the merge kernel may be scheduled now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ring = warp / kWPR, half = warp % kWPR;
-  const int SUB = a.B / BT;
+  const int NA = HPG * kWPH;                 // active warps per ring
+  const int ring = warp / kRingWarps, task = warp % kRingWarps;
+  const bool active = task < NA;
+  const int h_local = task / kWPH, slice = task % kWPH;
 
   // ---- per-sequence tile counts and prefix ----
   int carry = 0;
@@ -167,12 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
     int tiles_b = 0;
     if (b < a.batch) {
       int T = a.seq_lens[b];
-      if (T < 0 || T > a.max_blocks * a.B) {
+      if (T < 0 || T > a.max_blocks * B) {
         latch_error(a.err, KVSEL_ERR_BOUNDS);
-        T = T < 0 ? 0 : a.max_blocks * a.B;
+        T = T < 0 ? 0 : a.max_blocks * B;
       }
       tlen_s[b] = T;
-      const int N = (T + a.B - 1) / a.B;
+      const int N = (T + B - 1) / B;
       int nb;
       if (a.dense_flag && a.dense_flag[b]) {
         nb = N;
@@ -181,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
         if (nb < 0 || nb > a.k_max) latch_error(a.err, KVSEL_ERR_BOUNDS);
         nb = max(0, min(nb, min(N, a.k_max)));
       }
-      tiles_b = nb * SUB * a.Hkv;
+      tiles_b = nb * a.n_groups;
     }
     int x = tiles_b;
 #pragma unroll
@@ -204,6 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
   if (tid == 0) base_s[a.batch] = carry;
   __syncthreads();
   const int64_t total = carry;
+  const int A = int(min(int64_t(gridDim.x), max(int64_t(1), (total + kMinTilesPerCta - 1) / kMinTilesPerCta)));
+  if (blockIdx.x == 0) {
+    for (int i = tid; i <= a.batch; i += kThreads) a.meta[2 + i] = base_s[i];
+    if (tid == 0) {
+      a.meta[0] = int(total);
+      a.meta[1] = A;
+    }
+  }
 
   // sequences with nothing to attend: out = 0, lse = -inf
   for (int64_t e = int64_t(blockIdx.x) * kThreads + tid; e < int64_t(a.batch) * a.Hq;
@@ -217,53 +239,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
     }
   }
   if (total == 0) return;
-  const int A = int(min(int64_t(gridDim.x), max(int64_t(1), (total + kMinTilesPerCta - 1) / kMinTilesPerCta)));
   if (int(blockIdx.x) >= A) return;
   const int64_t g0 = total * blockIdx.x / A;
   const int64_t g1 = total * (blockIdx.x + 1) / A;
   if (g0 >= g1) return;
+  const int L = int(g1 - g0);
 
   if (tid == 0) {
-    for (int i = 0; i < S * kRings; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < S * kRings; ++i) {
+      mbar_init(&bars[i], 1);
+      done_s[i] = 0;
+    }
     fence_barrier_init();
-    prefetch_tensormap(&tmKV);
   }
   __syncthreads();
 
   // ---- this ring's tile stream: tiles g0 + ring + m * kRings ----
-  const int64_t L = g1 - g0;
-  const int count_r = L > ring ? int((L - ring + kRings - 1) / kRings) : 0;
+  const int LR = L > ring ? (L - ring + kRings - 1) / kRings : 0;
   const uint32_t tiles_base = smem_u32(tiles);
-  auto slot_off = [&](int m) -> int { return ((m % S) * kRings + ring) * kStageBytes; };
-  auto slot_bar = [&](int m) -> uint64_t* { return &bars[(m % S) * kRings + ring]; };
-  const bool leader = (half == 0);
-  auto ring_sync = [&]() {
-    if constexpr (kWPR > 1) {
-      asm volatile("bar.sync %0, %1;" ::"r"(1 + ring), "r"(kWPR * 32) : "memory");
-    } else {
-      __syncwarp();
-    }
-  };
-  int issued = 0;
-  bool dead = false;
-  // Tile descriptors, 32 at a time: lane i holds the TMA rows and the valid
-  // token count of the ring's tile (cbase + i) in `cur` and of tile
-  // (cbase + 32 + i) in `nxt`. Their block-table and selection loads are
-  // issued a whole batch ahead, so no global load sits between a tile's
-  // consumption and the next copy.
+  auto slot_idx = [&](int m) -> int { return (m % S) * kRings + ring; };
+  auto slot_bar = [&](int m) -> uint64_t* { return &bars[slot_idx(m)]; };
+  // Tile descriptors, 32 at a time: lane i holds the copy unit and valid token
+  // count of tile (cbase + i) in `cur` and of tile (cbase + 32 + i) in `nxt`;
+  // their selection and block-table loads run a whole batch ahead.
   int cbase = 0;
   int cur_rk = 0, cur_cnt = 0, nxt_rk = 0, nxt_cnt = 0;
   auto load_batch = [&](int base, int& rk, int& cnt) {
     const int m = base + lane;
     rk = cnt = 0;
-    if (m < count_r) {
-      const Tile t = tile_info<BT>(a, base_s, tlen_s, g0 + ring + int64_t(m) * kRings, leader);
-      rk = t.rk;
-      cnt = t.ok ? max(t.cnt, 0) : 0;
-    }
+    if (m < LR) tile_info(a, base_s, tlen_s, g0 + ring + int64_t(m) * kRings, task == 0, rk, cnt);
   };
-  // all lanes: descriptor of ring tile m, with cbase <= m < cbase + 64
-  auto tile_desc = [&](int m, int& rk, int& cnt) {
+  auto tile_desc = [&](int m, int& rk, int& cnt) {   // all lanes; cbase <= m < cbase + 64
     const int i = m - cbase;
     const int src = i & 31;
     const int rk0 = __shfl_sync(0xffffffffu, cur_rk, src), rk1 = __shfl_sync(0xffffffffu, nxt_rk, src);
@@ -271,392 +277,377 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(
     rk = i < 32 ? rk0 : rk1;
     cnt = i < 32 ? c0 : c1;
   };
-  // one 4-D box brings the K and V halves of a tile: [kv][half][row][64 channels]
-  auto issue = [&](int m, int rk) {   // ring leader, lane 0 only
+  auto issue = [&](int m, int unit) {   // one lane
     uint64_t* bar = slot_bar(m);
-    mbar_arrive_expect_tx(bar, kStageBytes);
-    tma_load_4d(tiles + slot_off(m), &tmKV, 0, rk, 0, 0, bar);
+    mbar_arrive_expect_tx(bar, uint32_t(tile_bytes));
+    unsigned char* dst = tiles + size_t(slot_idx(m)) * tile_bytes;
+    const kvsel_bf16* ksrc = a.k_base + int64_t(unit) * plane_elems;
+    const kvsel_bf16* vsrc = a.kind == KVSEL_KV_PAGED ? a.v_base + int64_t(unit) * plane_elems
+                                                        : ksrc + int64_t(a.n_groups) * plane_elems;
+    bulk_load(dst, ksrc, uint32_t(plane_bytes), bar);
+    bulk_load(dst + plane_bytes, vsrc, uint32_t(plane_bytes), bar);
   };
-  load_batch(0, cur_rk, cur_cnt);
-  load_batch(32, nxt_rk, nxt_cnt);
-  for (int m = 0; m < min(S, count_r); ++m) {
-    int rk, cnt;
-    tile_desc(m, rk, cnt);
-    if (leader && lane == 0) issue(m, rk);
+  if (active) {
+    load_batch(0, cur_rk, cur_cnt);
+    load_batch(32, nxt_rk, nxt_cnt);
   }
-  issued = min(S, count_r);
+  if (task == 0) {
+    for (int m = 0; m < min(S, LR); ++m) {
+      int rk, cnt;
+      tile_desc(m, rk, cnt);
+      if (lane == 0) issue(m, rk);
+    }
+  }
+  bool dead = false;
   int m_cur = 0;
 
   const int gq = lane >> 2, tq = lane & 3;   // mma group / thread-in-group
-  const int r0 = half * 16;                  // this warp's 16 token rows of each tile
+  const int r0 = slice * 16;                 // this warp's 16 token rows of its head
   int64_t g = g0;
   while (g < g1) {
-    // ---- segment (b, j) containing g ----
+    // ---- segment (sequence b, head group hg) containing g ----
     const int b = find_seq(base_s, a.batch, g);
-    const int seg_tiles = (base_s[b + 1] - base_s[b]) / a.Hkv;
-    const int j = int((g - base_s[b]) / seg_tiles);
-    const int64_t s_start = base_s[b] + int64_t(j) * seg_tiles;
+    const int seg_tiles = (base_s[b + 1] - base_s[b]) / a.n_groups;
+    const int hg = int((g - base_s[b]) / seg_tiles);
+    const int64_t s_start = base_s[b] + int64_t(hg) * seg_tiles;
     const int64_t s_end = s_start + seg_tiles;
     const int64_t sg1 = min(g1, s_end);
-    const bool owned = (s_start >= g0 && s_end <= g1);
+    const int head = hg * HPG + h_local;      // this warp's KV head
 
-    // Q fragments (rows >= G are zero)
-    uint32_t qa[kKS][4];
-    {
-      const kvsel_bf16* qb = a.q + (int64_t(b) * a.Hq + int64_t(j) * G) * D;
+    // O^T accumulators: o[mt][n] holds channels mt*16 + {g, g+8} of query heads
+    // n*8 + {2t, 2t+1}; mh / lh: running max and (per-thread) sum of those heads
+    float o[kMT][NTH][4];
 #pragma unroll
-      for (int ks = 0; ks < kKS; ++ks) {
-        const int c = ks * 16 + 2 * tq;
-        qa[ks][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qb + gq * D + c) : 0u;
-        qa[ks][1] = gq + 8 < G ? *reinterpret_cast<const uint32_t*>(qb + (gq + 8) * D + c) : 0u;
-        qa[ks][2] = gq < G ? *reinterpret_cast<const uint32_t*>(qb + gq * D + c + 8) : 0u;
-        qa[ks][3] = gq + 8 < G ? *reinterpret_cast<const uint32_t*>(qb + (gq + 8) * D + c + 8) : 0u;
-      }
-    }
-    float o[kNT][4];
+    for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
-    for (int nt = 0; nt < kNT; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-    float mrow[2] = {-INFINITY, -INFINITY};
-    float lrow[2] = {0.f, 0.f};
+      for (int n = 0; n < NTH; ++n) o[mt][n][0] = o[mt][n][1] = o[mt][n][2] = o[mt][n][3] = 0.f;
+    float mh[NTH][2], lh[NTH][2];
+#pragma unroll
+    for (int n = 0; n < NTH; ++n) mh[n][0] = mh[n][1] = -INFINITY, lh[n][0] = lh[n][1] = 0.f;
 
-    while (m_cur < count_r && g0 + ring + int64_t(m_cur) * kRings < sg1) {
-      if (m_cur == cbase + 32) {           // advance the descriptor window
-        cbase += 32;
-        cur_rk = nxt_rk; cur_cnt = nxt_cnt;
-        load_batch(cbase + 32, nxt_rk, nxt_cnt);
-      }
-      int t_rk, t_cnt;
-      tile_desc(m_cur, t_rk, t_cnt);
-      if (!dead && !mbar_wait_bounded(slot_bar(m_cur), uint32_t((m_cur / S) & 1))) {
-        dead = true;
-        if (lane == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
-      }
-      const int cnt = t_cnt - r0;            // valid tokens in this warp's 16 rows
-      if (!dead && cnt > 0) {
-        const int k_off = a.kv_swap ? kTileBytes : 0, v_off = a.kv_swap ? 0 : kTileBytes;
-        const uint32_t kt_base = tiles_base + slot_off(m_cur) + k_off;
-        const uint32_t vt_base = tiles_base + slot_off(m_cur) + v_off;
-        if (cnt < 16) {
-          // rows past the sequence end: zero V so that 0 * garbage cannot poison P V
-          unsigned char* vt = tiles + slot_off(m_cur) + v_off;
-          for (int idx = lane; idx < (16 - cnt) * (D / 8); idx += 32) {
-            const int row = r0 + cnt + idx / (D / 8);
-            const int c = (idx % (D / 8)) * 8;
-            *reinterpret_cast<uint4*>(vt + swz<BT>(0, row, c)) = make_uint4(0, 0, 0, 0);
-          }
-          __syncwarp();
-        }
-        // S = Q K^T over 16 tokens: two n-tiles, even / odd k-steps in separate
-        // accumulators so that four independent mma chains are in flight
-        float sa[2][4], sb[2][4];
+    if (active) {
+      // Q^T as the B operand: qb[ks][n] = q[head n*8 + g][ks*16 + {2t, 2t+1, 2t+8, 2t+9}]
+      // (query heads >= G are zero columns)
+      uint32_t qb[kKS][NTH][2];
+      {
+        const kvsel_bf16* qp = a.q + (int64_t(b) * a.Hq + int64_t(head) * G) * D;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
-        {
-          const int row = r0 + (lane & 7) + ((lane >> 4) << 3);
-          const int cofs = ((lane >> 3) & 1) * 8;
+        for (int n = 0; n < NTH; ++n) {
+          const int hq = n * 8 + gq;
 #pragma unroll
           for (int ks = 0; ks < kKS; ++ks) {
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(swz<BT>(kt_base, row, ks * 16 + cofs), b0, b1, b2, b3);
-            if (ks & 1) {
-              mma_bf16_16816(sb[0], qa[ks], b0, b1);
-              mma_bf16_16816(sb[1], qa[ks], b2, b3);
-            } else {
-              mma_bf16_16816(sa[0], qa[ks], b0, b1);
-              mma_bf16_16816(sa[1], qa[ks], b2, b3);
+            const int c = ks * 16 + 2 * tq;
+            qb[ks][n][0] = hq < G ? *reinterpret_cast<const uint32_t*>(qp + hq * D + c) : 0u;
+            qb[ks][n][1] = hq < G ? *reinterpret_cast<const uint32_t*>(qp + hq * D + c + 8) : 0u;
+          }
+        }
+      }
+      while (m_cur < LR && g0 + ring + int64_t(m_cur) * kRings < sg1) {
+        if (m_cur == cbase + 32) {             // advance the descriptor window
+          cbase += 32;
+          cur_rk = nxt_rk; cur_cnt = nxt_cnt;
+          load_batch(cbase + 32, nxt_rk, nxt_cnt);
+        }
+        int t_rk, t_cnt;
+        tile_desc(m_cur, t_rk, t_cnt);
+        if (!dead && !mbar_wait_bounded(slot_bar(m_cur), uint32_t((m_cur / S) & 1))) {
+          dead = true;
+          if (lane == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
+        }
+        const int cnt = t_cnt - slice * 16;    // valid tokens in this warp's 16 rows
+        const uint32_t st = tiles_base + uint32_t(slot_idx(m_cur)) * uint32_t(tile_bytes);
+        if (!dead && cnt > 0) {
+          if (cnt < 16) {
+            // rows past the sequence end: zero V so that 0 * garbage cannot poison P V
+            for (int idx = lane; idx < (16 - cnt) * (D / 8); idx += 32) {
+              const int row = r0 + cnt + idx / (D / 8);
+              const int c = (idx % (D / 8)) * 8;
+              const uint32_t ad = swz(st, plane_bytes, 1, h_local, kHalves, B, row, c);
+              asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(ad), "r"(0u) : "memory");
+            }
+            __syncwarp();
+          }
+          // S^T = K Q^T over this warp's 16 tokens (tokens are the M rows): even and
+          // odd k-steps in separate accumulators to shorten the mma chains
+          float sa[NTH][4], sb[NTH][4];
+#pragma unroll
+          for (int n = 0; n < NTH; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sa[n][e] = sb[n][e] = 0.f;
+          {
+            const int row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int cofs = (lane >> 4) * 8;
+#pragma unroll
+            for (int ks = 0; ks < kKS; ++ks) {
+              uint32_t ka[4];
+              ldsm_x4(swz(st, plane_bytes, 0, h_local, kHalves, B, row, ks * 16 + cofs), ka[0], ka[1],
+                      ka[2], ka[3]);
+#pragma unroll
+              for (int n = 0; n < NTH; ++n) {
+                if (ks & 1) mma_bf16_16816(sb[n], ka, qb[ks][n][0], qb[ks][n][1]);
+                else mma_bf16_16816(sa[n], ka, qb[ks][n][0], qb[ks][n][1]);
+              }
+            }
+          }
+          // scale, mask; e & 1 selects head 2t / 2t+1, e >> 1 token g / g + 8
+          float x[NTH][4], mx[NTH][2];
+#pragma unroll
+          for (int n = 0; n < NTH; ++n) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = gq + 8 * (e >> 1);
+              x[n][e] = tok < cnt ? (sa[n][e] + sb[n][e]) * a.scale_log2 : -INFINITY;
+            }
+            mx[n][0] = fmaxf(x[n][0], x[n][2]);
+            mx[n][1] = fmaxf(x[n][1], x[n][3]);
+          }
+          bool grow = false;
+#pragma unroll
+          for (int n = 0; n < NTH; ++n)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+#pragma unroll
+              for (int off = 4; off < 32; off <<= 1)
+                mx[n][c] = fmaxf(mx[n][c], __shfl_xor_sync(0xffffffffu, mx[n][c], off));
+              grow |= mx[n][c] > mh[n][c];
+            }
+          if (__any_sync(0xffffffffu, grow)) {
+            // a running max moved: rescale the accumulators of every head
+#pragma unroll
+            for (int n = 0; n < NTH; ++n) {
+              float alpha[2];
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const float mn = fmaxf(mh[n][c], mx[n][c]);
+                const float m_use = (mn == -INFINITY) ? 0.f : mn;
+                alpha[c] = ex2(mh[n][c] - m_use);
+                mh[n][c] = mn;
+                lh[n][c] *= alpha[c];
+              }
+#pragma unroll
+              for (int mt = 0; mt < kMT; ++mt) {
+                o[mt][n][0] *= alpha[0]; o[mt][n][2] *= alpha[0];
+                o[mt][n][1] *= alpha[1]; o[mt][n][3] *= alpha[1];
+              }
+            }
+          }
+          // P^T (tokens x heads) as the B operand: bf16 high and low parts, each
+          // 8x8 block transposed from the accumulator layout with movmatrix
+          uint32_t ph[NTH][2], pl[NTH][2];
+#pragma unroll
+          for (int n = 0; n < NTH; ++n) {
+            const float mu0 = (mh[n][0] == -INFINITY) ? 0.f : mh[n][0];
+            const float mu1 = (mh[n][1] == -INFINITY) ? 0.f : mh[n][1];
+            float pv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pv[e] = ex2(x[n][e] - ((e & 1) ? mu1 : mu0));
+              lh[n][e & 1] += pv[e];
+            }
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const uint32_t hi = pack_bf16x2(pv[2 * k], pv[2 * k + 1]);
+              const uint32_t lo = pack_bf16x2(pv[2 * k] - bf16lo(hi), pv[2 * k + 1] - bf16hi(hi));
+              ph[n][k] = movmatrix_t(hi);
+              pl[n][k] = movmatrix_t(lo);
+            }
+          }
+          // O^T += V^T P^T: V^T m-tiles (16 channels x 16 tokens) by ldmatrix.trans,
+          // two m-tiles at a time, high parts then low parts
+          {
+            const int row = r0 + (lane & 7) + ((lane >> 4) << 3);
+            const int cofs = ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int mt = 0; mt < kMT; mt += 2) {
+              uint32_t va[2][4];
+#pragma unroll
+              for (int u = 0; u < 2; ++u)
+                ldsm_x4_t(swz(st, plane_bytes, 1, h_local, kHalves, B, row, (mt + u) * 16 + cofs),
+                          va[u][0], va[u][1], va[u][2], va[u][3]);
+#pragma unroll
+              for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int n = 0; n < NTH; ++n) mma_bf16_16816(o[mt + u][n], va[u], ph[n][0], ph[n][1]);
+#pragma unroll
+              for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int n = 0; n < NTH; ++n) mma_bf16_16816(o[mt + u][n], va[u], pl[n][0], pl[n][1]);
             }
           }
         }
-        float s[2][4];
-        float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = nt * 8 + 2 * tq + (e & 1);
-            const float x = tok < cnt ? (sa[nt][e] + sb[nt][e]) * a.scale_log2 : -INFINITY;
-            s[nt][e] = x;
-            mx[e >> 1] = fmaxf(mx[e >> 1], x);
-          }
-        float mu[2];
-        bool grow = false;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-          mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-          grow |= mx[r] > mrow[r];
+        // release the slot; the last warp to release it refills it S tiles ahead
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const int before = atomicAdd(&done_s[slot_idx(m_cur)], 1);
+          last = (before % NA) == NA - 1;
         }
-        if (__any_sync(0xffffffffu, grow)) {
-          // a running max moved: rescale the accumulators of every row
-          float alpha[2];
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float mn = fmaxf(mrow[r], mx[r]);
-            const float m_use = (mn == -INFINITY) ? 0.f : mn;
-            alpha[r] = ex2(mrow[r] - m_use);
-            mrow[r] = mn;
-            lrow[r] *= alpha[r];
-          }
-#pragma unroll
-          for (int nt = 0; nt < kNT; ++nt) {
-            o[nt][0] *= alpha[0]; o[nt][1] *= alpha[0];
-            o[nt][2] *= alpha[1]; o[nt][3] *= alpha[1];
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last && !dead && m_cur + S < LR) {
+          int rk, cnt2;
+          tile_desc(m_cur + S, rk, cnt2);
+          if (lane == 0) {
+            fence_proxy_async();
+            issue(m_cur + S, rk);
           }
         }
-#pragma unroll
-        for (int r = 0; r < 2; ++r) mu[r] = (mrow[r] == -INFINITY) ? 0.f : mrow[r];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float p = ex2(s[nt][e] - mu[e >> 1]);
-            s[nt][e] = p;
-            lrow[e >> 1] += p;
-          }
-        uint32_t ph[4], pl[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float x0 = s[i >> 1][(i & 1) * 2 + 0];
-          const float x1 = s[i >> 1][(i & 1) * 2 + 1];
-          ph[i] = pack_bf16x2(x0, x1);
-          pl[i] = pack_bf16x2(x0 - bf16lo(ph[i]), x1 - bf16hi(ph[i]));
-        }
-        {
-          const int row = r0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-          const int cofs = (lane >> 4) * 8;
-#pragma unroll
-          for (int dc = 0; dc < D / 16; ++dc) {
-            uint32_t v0, v1, v2, v3;
-            ldsm_x4_t(swz<BT>(vt_base, row, dc * 16 + cofs), v0, v1, v2, v3);
-            mma_bf16_16816(o[2 * dc], ph, v0, v1);
-            mma_bf16_16816(o[2 * dc + 1], ph, v2, v3);
-            mma_bf16_16816(o[2 * dc], pl, v0, v1);
-            mma_bf16_16816(o[2 * dc + 1], pl, v2, v3);
-          }
-        }
+        ++m_cur;
       }
-      // release the slot (both warps of the ring are done) and refill it S tiles ahead
-      ring_sync();
-      if (!dead && m_cur + S < count_r) {
-        int rk, cnt2;
-        tile_desc(m_cur + S, rk, cnt2);
-        if (leader && lane == 0) {
-          fence_proxy_async();
-          issue(m_cur + S, rk);
-        }
-        issued = m_cur + S + 1;
-      }
-      ++m_cur;
     }
 
-    // ---- merge the warps' states for this segment ----
+    // ---- store this warp's state for the segment; the merge kernel combines ----
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-      lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-    }
-    {
-      float* mw = merge + warp * G * (D + 2);
+    for (int n = 0; n < NTH; ++n)
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int row = gq + 8 * r;
-        if (row < G) {
-          float* dst = mw + row * (D + 2);
-          if (tq == 0) {
-            dst[0] = mrow[r];
-            dst[1] = lrow[r];
-          }
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int nt = 0; nt < kNT; ++nt) {
-            dst[2 + nt * 8 + 2 * tq] = o[nt][2 * r];
-            dst[2 + nt * 8 + 2 * tq + 1] = o[nt][2 * r + 1];
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int slot = (g0 >= s_start) ? 0 : 1;
-    float* part = a.partials + (int64_t(blockIdx.x) * 2 + slot) * G * (D + 2);
-    for (int e = tid; e < G * D; e += kThreads) {
-      const int r = e / D, c = e % D;
-      float ms = -INFINITY;
+        for (int off = 4; off < 32; off <<= 1) lh[n][c] += __shfl_xor_sync(0xffffffffu, lh[n][c], off);
+    if (active) {
+      const int64_t seg = int64_t(b) * a.n_groups + hg;
+      float* mw = a.partials + ((int64_t(blockIdx.x) + seg) * kW + warp) * G * (D + 2);
 #pragma unroll
-      for (int w = 0; w < kW; ++w) ms = fmaxf(ms, merge[(w * G + r) * (D + 2)]);
-      float l = 0.f, acc = 0.f;
-      if (ms != -INFINITY) {
+      for (int n = 0; n < NTH; ++n)
 #pragma unroll
-        for (int w = 0; w < kW; ++w) {
-          const float* src = merge + (w * G + r) * (D + 2);
-          const float f = ex2(src[0] - ms);
-          l += src[1] * f;
-          acc += src[2 + c] * f;
-        }
-      }
-      const int64_t orow = int64_t(b) * a.Hq + int64_t(j) * G + r;
-      if (owned) {
-        const float v = l > 0.f ? acc / l : 0.f;
-        a.out[orow * D + c] = v;
-        if (a.out_bf16) a.out_bf16[orow * D + c] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-        if (c == 0) a.lse[orow] = l > 0.f ? (ms + lg2(l)) * 0.6931471805599453f : -INFINITY;
-      } else {
-        float* pr = part + r * (D + 2);
-        if (c == 0) {
-          pr[0] = ms;
-          pr[1] = l;
-        }
-        pr[2 + c] = acc;
-      }
-    }
-    if (!owned) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0) {
-        const int64_t first_c = ((s_start + 1) * A - 1) / total;
-        const int64_t last_c = ((s_end) * A - 1) / total;
-        const uint32_t expect = uint32_t(last_c - first_c + 1);
-        const uint32_t before = atomicAdd(&a.tickets[b * a.Hkv + j], 1u);
-        if (before + 1 == expect) {
-          a.tickets[b * a.Hkv + j] = 0;   // leave the workspace zero-filled
-          __threadfence();
-        }
-        flag_s = (before + 1 == expect) ? int(first_c) : -1;
-        scan_s[0] = int(last_c);
-      }
-      __syncthreads();
-      if (flag_s >= 0) {
-        const int c_first = flag_s, c_last = scan_s[0];
-        for (int e = tid; e < G * D; e += kThreads) {
-          const int r = e / D, c = e % D;
-          float ms = -INFINITY;
-          for (int cc = c_first; cc <= c_last; ++cc) {
-            const int sl = (total * cc / A >= s_start) ? 0 : 1;
-            const float* pr = a.partials + ((int64_t(cc) * 2 + sl) * G + r) * (D + 2);
-            ms = fmaxf(ms, __ldcg(pr));
-          }
-          float l = 0.f, acc = 0.f;
-          if (ms != -INFINITY) {
-            for (int cc = c_first; cc <= c_last; ++cc) {
-              const int sl = (total * cc / A >= s_start) ? 0 : 1;
-              const float* pr = a.partials + ((int64_t(cc) * 2 + sl) * G + r) * (D + 2);
-              const float f = ex2(__ldcg(pr) - ms);
-              l += __ldcg(pr + 1) * f;
-              acc += __ldcg(pr + 2 + c) * f;
+        for (int c = 0; c < 2; ++c) {
+          const int hq = n * 8 + 2 * tq + c;
+          if (hq < G) {
+            float* dst = mw + hq * (D + 2);
+            if (gq == 0) {
+              dst[0] = mh[n][c];
+              dst[1] = lh[n][c];
+            }
+#pragma unroll
+            for (int mt = 0; mt < kMT; ++mt) {
+              dst[2 + mt * 16 + gq] = o[mt][n][c];
+              dst[2 + mt * 16 + gq + 8] = o[mt][n][c + 2];
             }
           }
-          const int64_t orow = int64_t(b) * a.Hq + int64_t(j) * G + r;
-          const float v = l > 0.f ? acc / l : 0.f;
-          a.out[orow * D + c] = v;
-          if (a.out_bf16) a.out_bf16[orow * D + c] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-          if (c == 0) a.lse[orow] = l > 0.f ? (ms + lg2(l)) * 0.6931471805599453f : -INFINITY;
         }
-      }
     }
-    __syncthreads();
     g = sg1;
   }
 
   // drain copies still in flight (only after a timeout)
-  if (dead && leader && lane == 0)
-    for (int m = m_cur; m < issued; ++m) (void)mbar_wait_bounded(slot_bar(m), uint32_t((m / S) & 1));
+  if (dead && lane == 0 && task == 0)
+    for (int m = m_cur; m < min(LR, m_cur + S); ++m)
+      (void)mbar_wait_bounded(slot_bar(m), uint32_t((m / S) & 1));
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// Tensor map over K and V together: dims (innermost first) are 64 channels,
-// cache rows (stride D*2 bytes), the D/64 channel halves (stride 128 bytes)
-// and K vs V (stride = distance between the two buffers). A box of
-// {64, BT, D/64, 2} with the 128-byte swizzle lands as [kv][half][row][64] in
-// shared memory, every 128-byte row swizzled by its row index.
-bool encode_map(CUtensorMap* m, const void* base, int64_t rows, int64_t kv_stride, int D, int BT) {
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[4] = {64u, cuuint64_t(rows), cuuint64_t(D / 64), 2u};
-  cuuint64_t strides[3] = {cuuint64_t(D) * 2, 128u, cuuint64_t(kv_stride)};
-  cuuint32_t box[4] = {64u, cuuint32_t(BT), cuuint32_t(D / 64), 2u};
-  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// A tensor map depends only on (address, rows, K/V distance, D, BT): cache the
-// encodings so that a decode loop over the same buffers does no host-side
-// encoding.
-struct MapEntry {
-  const void* base;
-  int64_t rows, kv_stride;
-  int D, BT;
-  CUtensorMap map;
-};
-std::mutex g_map_mu;
-MapEntry g_maps[64];
-int g_map_next = 0, g_map_n = 0;
-
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t kv_stride, int D, int BT) {
-  {
-    std::lock_guard<std::mutex> lk(g_map_mu);
-    for (int i = 0; i < g_map_n; ++i) {
-      const MapEntry& e = g_maps[i];
-      if (e.base == base && e.rows == rows && e.kv_stride == kv_stride && e.D == D && e.BT == BT) {
-        *m = e.map;
-        return true;
-      }
+// One warp per output row (sequence b, query head h): log-sum-exp merge of the
+// states every warp stored for the row's segment. Launched as a programmatic
+// dependent of the decode kernel: it can be resident early and waits for the
+// decode grid's completion before it reads anything that grid wrote.
+template <int D>
+__global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a, int wph) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (row >= int64_t(a.batch) * a.Hq) return;
+  const int b = int(row / a.Hq), hq = int(row % a.Hq);
+  const int* base = a.meta + 2;
+  const int64_t total = a.meta[0];
+  const int A = a.meta[1];
+  const int t0 = __ldcg(base + b), t1 = __ldcg(base + b + 1);
+  if (t1 == t0) return;                   // no attended token: written by the decode kernel
+  const int G = a.G, j = hq / G, r = hq % G;
+  const int hg = j / a.hpg, h_local = j % a.hpg;
+  const int seg_tiles = (t1 - t0) / a.n_groups;
+  const int64_t s_start = t0 + int64_t(hg) * seg_tiles, s_end = s_start + seg_tiles;
+  const int first_c = int(((s_start + 1) * A - 1) / total);
+  const int last_c = int((s_end * A - 1) / total);
+  const int64_t seg = int64_t(b) * a.n_groups + hg;
+  const int per_cta = kRings * wph;       // warps of one CTA holding this head
+  const int NP = (last_c - first_c + 1) * per_cta;
+  auto state = [&](int i) -> const float* {
+    const int c = first_c + i / per_cta, k = i % per_cta;
+    const int w = (k / wph) * kRingWarps + h_local * wph + (k % wph);
+    return a.partials + (((int64_t(c) + seg) * kW + w) * G + r) * (D + 2);
+  };
+  float mloc = -INFINITY;
+  for (int i = lane; i < NP; i += 32) mloc = fmaxf(mloc, __ldcg(state(i)));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+  const float ms = mloc;
+  float lloc = 0.f;
+  if (ms != -INFINITY)
+    for (int i = lane; i < NP; i += 32) {
+      const float* st = state(i);
+      lloc += __ldcg(st + 1) * ex2(__ldcg(st) - ms);
+    }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
+  constexpr int kCPL = D / 32;            // channels per lane
+  float acc[kCPL];
+#pragma unroll
+  for (int u = 0; u < kCPL; ++u) acc[u] = 0.f;
+  if (ms != -INFINITY) {
+#pragma unroll 4
+    for (int i = 0; i < NP; ++i) {
+      const float* st = state(i);
+      const float f = ex2(__ldcg(st) - ms);
+#pragma unroll
+      for (int u = 0; u < kCPL; ++u) acc[u] += f * __ldcg(st + 2 + lane * kCPL + u);
     }
   }
-  if (!encode_map(m, base, rows, kv_stride, D, BT)) return false;
-  std::lock_guard<std::mutex> lk(g_map_mu);
-  MapEntry& e = g_maps[g_map_next];
-  e.base = base; e.rows = rows; e.kv_stride = kv_stride; e.D = D; e.BT = BT; e.map = *m;
-  g_map_next = (g_map_next + 1) % 64;
-  if (g_map_n < 64) ++g_map_n;
-  return true;
+  const float l = lloc;
+#pragma unroll
+  for (int u = 0; u < kCPL; ++u) {
+    const int c = lane * kCPL + u;
+    const float v = l > 0.f ? acc[u] / l : 0.f;
+    a.out[row * D + c] = v;
+    if (a.out_bf16) a.out_bf16[row * D + c] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  if (lane == 0) a.lse[row] = l > 0.f ? (ms + lg2(l)) * 0.6931471805599453f : -INFINITY;
 }
 
-template <int D, int BT>
-cudaError_t launch_t(const kvsel_problem& p, const DecodeArgs& a0, const CUtensorMap& mkv,
-                     cudaStream_t s) {
+template <int D, int B, int NTH>
+cudaError_t launch_t(const kvsel_problem& p, const DecodeArgs& a0, cudaStream_t s) {
   DecodeArgs a = a0;
-  constexpr int kRings = kW / (BT / 16);
-  constexpr int kGroupBytes = kRings * 2 * BT * D * 2;   // one stage of every ring
+  const size_t tile_bytes = size_t(a.hpg) * B * D * 4;
   // 1024: manual alignment of the tile area; 256: static shared variables
-  const size_t rest = 1024 + 256 + size_t(kW) * a.G * (D + 2) * 4 + (size_t(p.batch) * 2 + 1) * 4;
+  const size_t rest = 1024 + 256 + 8 * 2 * kMaxStages * kRings + (size_t(p.batch) * 2 + 1) * 4;
   const int max_optin = max_smem_optin();
-  int stages = int((size_t(max_optin) - rest - 8 * kRings * kMaxStages) / size_t(kGroupBytes));
+  int stages = int((size_t(max_optin) - rest - 8 * kMaxStages * kRings) / (tile_bytes * kRings));
   stages = std::min(kMaxStages, stages);
   if (stages < 1) return cudaErrorInvalidConfiguration;
   a.stages = stages;
-  const size_t smem = rest + size_t(stages) * kGroupBytes + 8 * kRings * stages;
-  auto kfn = sparse_decode_kernel<D, BT>;
+  const size_t smem = rest + size_t(stages) * kRings * tile_bytes + 8 * stages * kRings;
+  auto kfn = sparse_decode_kernel<D, B, NTH>;
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kfn), int(smem));
   if (e != cudaSuccess) return e;
   const int grid = std::min(kMaxCtas, sm_count());
-  kfn<<<grid, kThreads, smem, s>>>(mkv, a);
+  kfn<<<grid, kThreads, smem, s>>>(a);
   count_launch();
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the row merge, as a programmatic dependent of the decode grid
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((int64_t(p.batch) * p.n_qheads + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, merge_rows_kernel<D>, a, int(B / 16));
+  count_launch();
+  return e;
 }
 
 }  // namespace
 
+size_t decode_meta_bytes(const kvsel_problem& p) {
+  return (size_t(p.batch) * 4 + 3 * 4 + 255) / 256 * 256;
+}
+
 size_t sparse_decode_ws_bytes(const kvsel_problem& p) {
   const int G = p.n_qheads / std::max(1, p.n_kvheads);
-  const size_t tickets = (size_t(p.batch) * p.n_kvheads * 4 + 255) / 256 * 256;
-  const size_t parts = size_t(kMaxCtas) * 2 * G * (p.head_dim + 2) * 4;
-  return tickets + parts;
+  const int hpg = heads_per_group(p.block_size, p.n_kvheads);
+  const size_t segments = size_t(p.batch) * (p.n_kvheads / hpg);
+  const size_t parts = (size_t(kMaxCtas) + segments) * kW * G * (p.head_dim + 2) * 4;
+  return decode_meta_bytes(p) + parts;
 }
 
 cudaError_t launch_sparse_decode(const kvsel_problem& p, const kvsel_bf16* q,
@@ -674,33 +665,28 @@ cudaError_t launch_sparse_decode(const kvsel_problem& p, const kvsel_bf16* q,
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = out; a.out_bf16 = out_bf16; a.lse = lse;
   char* w = static_cast<char*>(ws);
-  a.tickets = reinterpret_cast<uint32_t*>(w);
-  a.partials = reinterpret_cast<float*>(w + (size_t(p.batch) * p.n_kvheads * 4 + 255) / 256 * 256);
+  a.meta = reinterpret_cast<int*>(w);
+  a.partials = reinterpret_cast<float*>(w + decode_meta_bytes(p));
+  a.hpg = heads_per_group(p.block_size, p.n_kvheads);
+  a.n_groups = p.n_kvheads / a.hpg;
   a.err = err;
   a.batch = p.batch; a.Hq = p.n_qheads; a.Hkv = p.n_kvheads; a.G = p.n_qheads / p.n_kvheads;
   a.B = p.block_size; a.max_blocks = p.max_blocks; a.k_max = p.k_max;
   const int D = p.head_dim;
-  const int BT = std::min(p.block_size, 32);
-  CUtensorMap mkv;
   if (a.kind == KVSEL_KV_PAGED) {
-    const int64_t rows = kv.n_pages * p.n_kvheads * p.block_size;
-    const char* kb = reinterpret_cast<const char*>(kv.k_pages);
-    const char* vb = reinterpret_cast<const char*>(kv.v_pages);
-    const int64_t dist = vb > kb ? int64_t(vb - kb) : int64_t(kb - vb);
-    a.kv_swap = vb < kb ? 1 : 0;
-    if (dist == 0 || (dist & 15) || dist >= (int64_t(1) << 40)) return cudaErrorInvalidValue;
-    if (!make_map(&mkv, a.kv_swap ? kv.v_pages : kv.k_pages, rows, dist, D, BT))
-      return cudaErrorInvalidValue;
+    a.k_base = kv.k_pages;
+    a.v_base = kv.v_pages;
   } else {
-    const int64_t rows = int64_t(p.batch) * kv.staging_slots * 2 * p.n_kvheads * p.block_size;
-    const int64_t dist = int64_t(p.n_kvheads) * p.block_size * D * 2;
-    a.kv_swap = 0;
-    if (!make_map(&mkv, kv.staging, rows, dist, D, BT)) return cudaErrorInvalidValue;
+    a.k_base = kv.staging;
+    a.v_base = nullptr;
   }
-  if (D == 128 && BT == 32) return launch_t<128, 32>(p, a, mkv, s);
-  if (D == 128 && BT == 16) return launch_t<128, 16>(p, a, mkv, s);
-  if (D == 64 && BT == 32) return launch_t<64, 32>(p, a, mkv, s);
-  if (D == 64 && BT == 16) return launch_t<64, 16>(p, a, mkv, s);
+  const int Bs = p.block_size;
+  if (D == 128 && Bs == 16) return a.G <= 8 ? launch_t<128, 16, 1>(p, a, s) : launch_t<128, 16, 2>(p, a, s);
+  if (D == 128 && Bs == 32) return a.G <= 8 ? launch_t<128, 32, 1>(p, a, s) : launch_t<128, 32, 2>(p, a, s);
+  if (D == 128 && Bs == 64) return a.G <= 8 ? launch_t<128, 64, 1>(p, a, s) : launch_t<128, 64, 2>(p, a, s);
+  if (D == 64 && Bs == 16) return a.G <= 8 ? launch_t<64, 16, 1>(p, a, s) : launch_t<64, 16, 2>(p, a, s);
+  if (D == 64 && Bs == 32) return a.G <= 8 ? launch_t<64, 32, 1>(p, a, s) : launch_t<64, 32, 2>(p, a, s);
+  if (D == 64 && Bs == 64) return a.G <= 8 ? launch_t<64, 64, 1>(p, a, s) : launch_t<64, 64, 2>(p, a, s);
   return cudaErrorInvalidValue;
 }
 

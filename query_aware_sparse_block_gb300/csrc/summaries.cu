@@ -19,6 +19,13 @@ namespace {
 
 constexpr int kThreads = 128;
 
+// Element offset, inside one (page, head) tile of the tiled layout, of the
+// 8-channel vector starting at channel c0 (c0 % 8 == 0) of token row t.
+__device__ __forceinline__ int64_t tiled_off(int t, int c0, int B) {
+  const int half = c0 >> 6, chunk = (c0 & 63) >> 3;
+  return (int64_t(half) * B + t) * 64 + ((chunk ^ (t & 7)) << 3);
+}
+
 __device__ __forceinline__ uint16_t f64_to_bf16_rne(double x) {
   float f = __double2float_rz(x);
   if (static_cast<double>(f) != x) f = __uint_as_float(__float_as_uint(f) | 1u);  // round to odd
@@ -46,7 +53,7 @@ __device__ __forceinline__ uint4 mean_to_bf16x8(const double (&acc)[8], int cnt)
 }
 
 // One CTA per (block n, sequence b). Threads own 8-channel column vectors of
-// one KV head and walk the block's tokens in order.
+// one KV head and walk the block's tokens in order (pages in the tiled layout).
 __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
     const kvsel_bf16* __restrict__ k_pages, int64_t n_pages, const int32_t* __restrict__ block_table,
     const int32_t* __restrict__ seq_lens, kvsel_bf16* __restrict__ summaries,
@@ -76,7 +83,7 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
   for (int v = threadIdx.x; v < n_vec; v += blockDim.x) {
     const int j = v / vec_per_head;
     const int c0 = (v % vec_per_head) * 8;
-    const kvsel_bf16* src = k_pages + ((page * H + j) * B) * int64_t(d) + c0;
+    const kvsel_bf16* tile = k_pages + (page * H + j) * int64_t(B) * d;
     double acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0;
@@ -84,7 +91,7 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
     for (; t + 8 <= cnt; t += 8) {
       uint4 r[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) r[u] = ldg_stream(src + int64_t(t + u) * d);
+      for (int u = 0; u < 8; ++u) r[u] = ldg_stream(tile + tiled_off(t + u, c0, B));
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         double x[8];
@@ -95,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
     }
     for (; t < cnt; ++t) {
       double x[8];
-      unpack8(ldg_stream(src + int64_t(t) * d), x);
+      unpack8(ldg_stream(tile + tiled_off(t, c0, B)), x);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] += x[i];
     }
@@ -136,7 +143,7 @@ __global__ void __launch_bounds__(kThreads) summaries_append_kernel(
   for (int v = threadIdx.x; v < n_vec; v += blockDim.x) {
     const int j = v / vec_per_head;
     const int c0 = (v % vec_per_head) * 8;
-    const int64_t cache_off = ((page * H + j) * B + row) * int64_t(d) + c0;
+    const int64_t cache_off = (page * H + j) * int64_t(B) * d + tiled_off(row, c0, B);
     const int64_t tok_off = (int64_t(b) * H + j) * d + c0;
     uint4 kv;
     if (new_k) {

@@ -16,7 +16,7 @@ import oracle as o
 from tests._parity import (attn_errors, check_sequence, default_scale, seq_inputs, selection_verdict,
                            to_dev)
 from workloads import C0, C1, C2, C3, C4, Workload
-from workloads.generate import bits, generate_layer, host_tier_layout, logical_kv
+from workloads.generate import bits, generate_layer, host_tier_layout, logical_kv, natural_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -259,8 +259,8 @@ def test_c4_offload_tier_fetch_then_decode(K):
     k = w.k_for(w.keep_floor)
     x = generate_layer(w, 0, device="cuda:0", perm=False)
     N = w.n_blocks
-    host = torch.empty((w.batch, N, 2, w.n_kvheads, w.block_size, w.head_dim), dtype=torch.bfloat16,
-                       pin_memory=True)
+    tile = tuple(x["k_pages"].shape[1:])
+    host = torch.empty((w.batch, N, 2) + tile, dtype=torch.bfloat16, pin_memory=True)
     host_tier_layout(x["k_pages"], x["v_pages"], x["block_table"], N, out=host)
     dec = _decoder(w, x, k_max=N)
     summ, acc = dec.new_summaries()
@@ -270,16 +270,15 @@ def test_c4_offload_tier_fetch_then_decode(K):
     dec.k_per_seq.fill_(k)
     dec.select(x["q"], summ, x["seq_lens"], gamma=w.gamma)
     slots = k
-    staging = torch.empty((w.batch, slots, 2, w.n_kvheads, w.block_size, w.head_dim),
-                          dtype=torch.bfloat16, device="cuda:0")
+    staging = torch.empty((w.batch, slots, 2) + tile, dtype=torch.bfloat16, device="cuda:0")
     from query_aware_sparse_block_gb300 import kvsel as KK
     kv = KK.kv_host(host, N, staging, slots)
     dec.attend(x["q"], kv, x["seq_lens"])
     torch.cuda.synchronize()
     for b in (0, 31, 63):
         qb = bits(x["q"][b])
-        kb = bits(host[b, :, 0].permute(0, 2, 1, 3).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
-        vb = bits(host[b, :, 1].permute(0, 2, 1, 3).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
+        kb = bits(natural_blocks(host[b, :, 0]).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
+        vb = bits(natural_blocks(host[b, :, 1]).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
         sb, _, _ = o.block_summaries(kb, w.seq_len, w.block_size)
         sc = o.block_scores(qb, sb)
         gsel = dec.sel_idx[b, : int(dec.n_sel[b])].cpu().numpy()

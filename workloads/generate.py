@@ -12,10 +12,14 @@ draws q, then K, then V, each ~N(0, 1) in fp32 and rounded to bf16. Then:
   * drift: K[t, j, c] += amp * sin(2*pi*t/period + 2*pi*(j*d + c)/(H_kv*d)),
     added in fp32 before the bf16 rounding.
 
-Device layout (paged cache): K and V pages are [n_pages][H_kv][B][d] bf16; the
-block table [batch][max_blocks] int32 maps a sequence's logical block to its
-page. ``perm=True`` scatters logical blocks over pages in a seeded random
-order so that every path goes through the table.
+Device layout (paged cache): K and V pages are [n_pages][H_kv][d/64][B][64]
+bf16 -- each (page, KV head) tile stores its B x d keys as d/64 column halves
+of B rows x 64 channels, and within every 128-byte row the 16-byte chunk c of
+token row t sits at chunk position c ^ (t % 8). ``to_tiled`` / ``from_tiled``
+convert between that and the natural [..., B, d] order. The block table
+[batch][max_blocks] int32 maps a sequence's logical block to its page.
+``perm=True`` scatters logical blocks over pages in a seeded random order so
+that every path goes through the table.
 """
 from __future__ import annotations
 
@@ -35,6 +39,34 @@ def _gen(seed: int, device) -> torch.Generator:
 
 def _randn_bf16(shape, g, device) -> torch.Tensor:
     return torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+
+
+def _chunk_swizzle(y: torch.Tensor) -> torch.Tensor:
+    """[..., B, 8 chunks, 8] -> same shape with chunk c of row t moved to c ^ (t % 8).
+
+    XOR is its own inverse, so the same routine un-swizzles.
+    """
+    B = y.shape[-3]
+    out = torch.empty_like(y)
+    for r in range(8):
+        perm = torch.tensor([c ^ r for c in range(8)], device=y.device)
+        out[..., r::8, :, :] = y[..., r::8, :, :].index_select(-2, perm)
+    return out
+
+
+def to_tiled(x: torch.Tensor) -> torch.Tensor:
+    """Natural [..., B, d] tiles -> the cache layout [..., d/64, B, 64]."""
+    *lead, B, d = x.shape
+    h2 = d // 64
+    y = x.reshape(*lead, B, h2, 8, 8).movedim(-3, -4)        # [..., h2, B, 8, 8]
+    return _chunk_swizzle(y).reshape(*lead, h2, B, 64)
+
+
+def from_tiled(y: torch.Tensor) -> torch.Tensor:
+    """Cache layout [..., d/64, B, 64] -> natural [..., B, d]."""
+    *lead, h2, B, _ = y.shape
+    x = _chunk_swizzle(y.reshape(*lead, h2, B, 8, 8))        # [..., h2, B, 8, 8]
+    return x.movedim(-4, -3).reshape(*lead, B, h2 * 64)
 
 
 def generate_layer(w: Workload, layer: int = 0, device="cpu", max_blocks: int | None = None,
@@ -77,12 +109,13 @@ def generate_layer(w: Workload, layer: int = 0, device="cpu", max_blocks: int | 
     else:
         page_of = torch.arange(n_pages, dtype=torch.int32)
     block_table = page_of.view(b, MB).to(device)
-    k_pages = torch.empty((n_pages, Hkv, B, d), dtype=torch.bfloat16, device=device)
+    k_pages = torch.empty((n_pages, Hkv, d // 64, B, 64), dtype=torch.bfloat16, device=device)
     v_pages = torch.empty_like(k_pages)
     idx = page_of.to(device=device, dtype=torch.long)
-    k_pages[idx] = kb.view(n_pages, Hkv, B, d)
-    v_pages[idx] = vb.view(n_pages, Hkv, B, d)
-    del kb, vb
+    k_pages[idx] = to_tiled(kb.view(n_pages, Hkv, B, d))
+    del kb
+    v_pages[idx] = to_tiled(vb.view(n_pages, Hkv, B, d))
+    del vb
     if seq_lens is None:
         seq_lens = torch.full((b,), w.seq_len, dtype=torch.int32)
     seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32).to(device)
@@ -97,20 +130,25 @@ def bits(t: torch.Tensor) -> np.ndarray:
 
 def logical_kv(pages: torch.Tensor, block_table: torch.Tensor, b: int, T: int) -> torch.Tensor:
     """One sequence's cache in token order [T][H_kv][d], gathered from its pages."""
-    B = pages.shape[2]
+    B = pages.shape[3]
     N = (T + B - 1) // B
     p = block_table[b, :N].long().to(pages.device)
-    blk = pages[p]                                  # [N][H_kv][B][d]
-    return blk.permute(0, 2, 1, 3).reshape(N * B, pages.shape[1], pages.shape[3])[:T]
+    blk = from_tiled(pages[p])                      # [N][H_kv][B][d]
+    return blk.permute(0, 2, 1, 3).reshape(N * B, blk.shape[1], blk.shape[3])[:T]
+
+
+def natural_blocks(tiles: torch.Tensor) -> torch.Tensor:
+    """[..., H_kv, d/64, B, 64] cache tiles -> token-major [..., B, H_kv, d]."""
+    x = from_tiled(tiles)                           # [..., H_kv, B, d]
+    return x.transpose(-3, -2)
 
 
 def host_tier_layout(k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
                      n_blocks: int, out: torch.Tensor | None = None) -> torch.Tensor:
-    """Offload-tier layout [b][N][2][H_kv][B][d]: K then V of one block contiguous."""
+    """Offload-tier layout [b][N][2][page tile]: K then V of one block contiguous."""
     b = block_table.shape[0]
-    _, Hkv, B, d = k_pages.shape
     if out is None:
-        out = torch.empty((b, n_blocks, 2, Hkv, B, d), dtype=torch.bfloat16)
+        out = torch.empty((b, n_blocks, 2) + tuple(k_pages.shape[1:]), dtype=torch.bfloat16)
     for s in range(b):
         p = block_table[s, :n_blocks].long().to(k_pages.device)
         out[s].copy_(torch.stack([k_pages[p], v_pages[p]], dim=1))
