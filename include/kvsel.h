@@ -138,10 +138,13 @@ KVSEL_API int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16
                           kvsel_bf16* summaries, double* open_acc, kvsel_stream_t stream);
 
 /*
- * kvsel_score_topk -- query-aware block score, Top-k and span merge in one
- * launch ("SparPR KV cache recovery on a consumer GPU", paragraphs
- * "Query-Aware key-block selection" and "On-demand local recomputation with
- * cost-aware fallback").
+ * kvsel_score_topk -- query-aware block score, Top-k and span merge
+ * ("SparPR KV cache recovery on a consumer GPU", paragraphs "Query-Aware
+ * key-block selection" and "On-demand local recomputation with cost-aware
+ * fallback"). Enqueues two kernels on `stream` (scores, then Top-k), each
+ * launched with programmatic stream serialization: a grid may become resident
+ * while the kernel before it still runs, but reads no input before that
+ * kernel has completed, so stream order is kept.
  *
  * score[b][n] = sum over query heads h of <q[b][h], summaries[b][n][kv(h)]>,
  * kv(h) = h / G, accumulated in fp32 (q is first folded over each GQA group).
@@ -157,7 +160,8 @@ KVSEL_API int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16
  * k_per_seq: device [batch] int32 (k_per_seq[b] > k_max latches BOUNDS and
  * is clamped). scores_out: device [batch][max_blocks] fp32, nullable.
  * dense_flag: device [batch] uint8, nullable. ws: workspace of
- * kvsel_workspace_size(p, KVSEL_WS_SCORE_TOPK) bytes.
+ * kvsel_workspace_size(p, KVSEL_WS_SCORE_TOPK) bytes (no initial contents
+ * required).
  */
 KVSEL_API int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_bf16* summaries,
                      const int32_t* seq_lens, const int32_t* k_per_seq, float gamma,
@@ -192,8 +196,8 @@ KVSEL_API int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, 
  * exceeds it (roughly batch * max_blocks > 1M) is rejected with
  * KVSEL_ERR_WORKSPACE and nothing is enqueued. The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture. Each call clears
- * the per-sequence tickets on `stream` before the kernel; no call allocates.
+ * current; make that first call before any stream capture. Nothing in the
+ * array needs to start at zero, so no call clears it; no call allocates.
  * All calls on a device share the one array, so calls that can overlap on
  * the GPU (different streams without ordering between them) race.
  */

@@ -187,4 +187,24 @@ __device__ __forceinline__ void stg_stream(void* p, uint4 v) {
                : "memory");
 }
 
+// Host: launch with programmatic stream serialization. The grid may become
+// resident while the previous kernel of the stream still runs; the kernel
+// executes griddepcontrol.wait before it reads any input, which returns once
+// every prerequisite grid has completed and its writes are visible.
+template <typename... Args>
+inline cudaError_t launch_pdl(void (*kfn)(Args...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kfn, args...);
+}
+
 }  // namespace kvsel

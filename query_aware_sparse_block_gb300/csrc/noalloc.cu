@@ -1,7 +1,8 @@
 // kvsel_score_topk_noalloc: the score + Top-k + span entry point for callers
-// that cannot allocate device memory themselves. Its scratch (per-sequence
-// tickets and the fp32 score row of every sequence) lives in a fixed
-// file-scope device array of this library instead of a caller workspace.
+// that cannot allocate device memory themselves. Its scratch (the fp32 score
+// row of every sequence) lives in a fixed file-scope device array of this
+// library instead of a caller workspace. Every score is written before it is
+// read within one call, so nothing in the array has to start at zero.
 //
 // The array is a device symbol: host code cannot use its name as an address.
 // Its device address is looked up once per device with cudaGetSymbolAddress,
@@ -68,13 +69,6 @@ KVSEL_API int kvsel_score_topk_noalloc(const kvsel_problem* p, const kvsel_bf16*
   cudaError_t e = kvsel::scratch_address(&scratch);
   if (e != cudaSuccess) {
     kvsel::set_last_error("score_topk_noalloc: scratch address: %s", cudaGetErrorString(e));
-    return KVSEL_ERR_CUDA;
-  }
-  // The tickets must start at zero; the array keeps whatever the last call left.
-  const size_t ticket_bytes = (size_t(p->batch) * 4 + 255) / 256 * 256;
-  e = cudaMemsetAsync(scratch, 0, ticket_bytes, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) {
-    kvsel::set_last_error("score_topk_noalloc: clearing the tickets: %s", cudaGetErrorString(e));
     return KVSEL_ERR_CUDA;
   }
   return kvsel_score_topk(p, q, summaries, seq_lens, k_per_seq, gamma, tau_rel, sel_idx, n_sel,

@@ -1,23 +1,30 @@
-// Query-aware block scoring, Top-k selection and span merge in one launch
+// Query-aware block scoring, Top-k selection and span merge
 // ("SparPR KV cache recovery on a consumer GPU": paragraph "Query-Aware
 // key-block selection" for the score and Top-k, paragraph "On-demand local
 // recomputation with cost-aware fallback" for spans and the Dense Fallback
 // Threshold gamma).
 //
-// Design (GB300): the summary table is the only large input, so the kernel is
-// a balanced stream over it. The flattened list of (sequence, block) pairs is
-// cut into equal contiguous ranges, one per CTA (one CTA per SM). A CTA's
-// range is cut into chunks of whole blocks of one sequence (contiguous in
-// memory); one thread moves each chunk into shared memory with a 1-D bulk
-// (TMA) copy, S chunks ahead, completions counted on mbarriers. Warps read
-// block summaries from shared memory, multiply by the query folded over its
-// GQA group (fp32, kept in registers) and reduce with shuffles. The last CTA
-// to finish a sequence (an atomic ticket per sequence; no CTA ever waits for
-// another) runs the Top-k on that sequence's scores: a 4-pass 8-bit radix
-// select (shared-memory histograms) finds the k-th largest key, ties at
-// that key are taken in index order, and block-wide scans emit the ascending
-// selection, the spans and the gamma decision. Tickets are reset by their
-// last user, so the workspace stays zero-filled between calls.
+// Design (GB300): two grids per call, chained by programmatic dependent
+// launch so that each is resident before its predecessor finishes.
+//
+// score_kernel streams the summary table, the only large input. The flattened
+// list of (sequence, block) pairs is cut into equal contiguous ranges, one per
+// CTA (one CTA per SM), with every cut moved to a chunk boundary of its
+// sequence. A CTA's range is cut into chunks of whole blocks of one sequence
+// (contiguous in memory); one thread moves each chunk into shared memory with
+// a 1-D bulk (TMA) copy, S chunks ahead, completions counted on mbarriers. The
+// query rows of a sequence ride along with the first chunk of that sequence
+// in the same stage, so folding q over its GQA group never waits on a global
+// load. Warps read block summaries from shared memory, multiply by the folded
+// query (fp32, in registers), reduce with shuffles and write one fp32 score
+// per block.
+//
+// select_kernel runs one CTA per sequence on those scores: a 2048-bin
+// histogram linear in the score value locates the bin holding the k-th
+// largest score and the few scores of that bin are ranked exactly (tied or
+// clustered rows fall back to a histogram search over the order keys), ties
+// at the k-th key are taken in index order, and block-wide scans emit the
+// ascending selection, the spans and the gamma decision.
 #include "kvsel_common.cuh"
 #include "kvsel_internal.h"
 
@@ -26,8 +33,12 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kStageBytes = 32 * 1024;
+constexpr int kStageBytes = 32 * 1024;   // summary bytes per stage (query rows follow)
 constexpr int kMaxStages = 4;
+constexpr int kBins = 2048;               // histogram bins of the Top-k threshold search
+constexpr int kBinsPerThread = kBins / kThreads;
+constexpr int kCand = 128;                // bin size ranked exactly instead of refined
+static_assert(kBins % kThreads == 0, "bins per thread");
 
 struct ScoreArgs {
   const kvsel_bf16* q;
@@ -42,12 +53,13 @@ struct ScoreArgs {
   int32_t* n_spans;
   uint8_t* dense_flag;
   float* scores;       // [batch][max_blocks]
-  uint32_t* tickets;   // [batch]
-  int* err;
+    int* err;
   int batch, Hq, Hkv, d, B, max_blocks, k_max;
   int NV, LPB;         // 16-byte vectors per block summary; lanes per block
   int chunk_blocks;    // blocks per bulk copy
   int stages;
+  int stage_bytes;     // kStageBytes + query bytes of one sequence
+  int sel_offset;      // byte offset of the Top-k key / flag area in dynamic shared memory
 };
 
 __device__ __forceinline__ int seq_blocks(const ScoreArgs& a, int b) {
@@ -61,6 +73,11 @@ __device__ __forceinline__ int seq_blocks(const ScoreArgs& a, int b) {
 __device__ __forceinline__ uint32_t order_key(float s) {
   uint32_t u = __float_as_uint(s + 0.0f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Inverse of order_key (-0 comes back as +0).
+__device__ __forceinline__ float key_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 // Block-wide exclusive scan of one int per thread; returns the prefix and the
@@ -87,10 +104,94 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* to
   return wsum + x - v;
 }
 
-// Top-k + spans + gamma decision for sequence b (whole CTA). keys_s holds
-// max_blocks + 2 uint32, flags_s max_blocks bytes.
-__device__ void select_sequence(const ScoreArgs& a, int b, uint32_t* keys_s, uint8_t* flags_s,
-                                int* hist_s, int* scratch_s, int* bcast_s) {
+struct SelectSmem {
+  uint32_t* keys;     // [max_blocks + 2] order keys (later: span starts / ends)
+  uint8_t* flags;     // [max_blocks] selection flags
+  int* hist;          // [kBins], all zero between uses
+  uint32_t* cand;     // [kCand] keys of the threshold bin
+  int* scratch;       // [kWarps] scan partials
+  uint32_t* mm;       // [2 * kWarps] min / max partials
+  int* bcast;         // [8]; bcast[7] is a gather counter, zero between uses
+};
+
+// After a histogram of the candidates' bins: the bin holding the r-th largest
+// candidate (bcast[0]), how many candidates lie in higher bins (bcast[1]) and
+// in that bin (bcast[2]). Clears the histogram. Two barriers.
+__device__ __forceinline__ void locate_bin(const SelectSmem& sm, int r) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int h[kBinsPerThread];
+  int tot = 0;
+#pragma unroll
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    h[j] = sm.hist[tid * kBinsPerThread + j];
+    sm.hist[tid * kBinsPerThread + j] = 0;
+    tot += h[j];
+  }
+  int x = tot;                                // suffix sum over this warp's threads
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, x, off);
+    if (lane + off < 32) x += y;
+  }
+  if (lane == 0) sm.scratch[warp] = x;
+  __syncthreads();
+  int above = x - tot;                        // candidates in higher bins
+  for (int w = warp + 1; w < kWarps; ++w) above += sm.scratch[w];
+#pragma unroll
+  for (int j = kBinsPerThread - 1; j >= 0; --j) {
+    if (above < r && above + h[j] >= r) {
+      sm.bcast[0] = tid * kBinsPerThread + j;
+      sm.bcast[1] = above;
+      sm.bcast[2] = h[j];
+    }
+    above += h[j];
+  }
+  __syncthreads();
+}
+
+// Rank the m (<= kCand) gathered candidates exactly: the r-th largest key
+// (bcast[4]), how many candidates exceed it (bcast[5]) and equal it
+// (bcast[6]). Resets the gather counter. One barrier after the gather's.
+__device__ __forceinline__ void rank_candidates(const SelectSmem& sm, int m, int r) {
+  const int tid = threadIdx.x;
+  if (tid < m) {
+    const uint32_t c = sm.cand[tid];
+    int g = 0, e = 0;
+    for (int j = 0; j < m; ++j) {
+      const uint32_t o = sm.cand[j];
+      g += o > c;
+      e += o == c;
+    }
+    if (g < r && r <= g + e) {
+      sm.bcast[4] = int(c);
+      sm.bcast[5] = g;
+      sm.bcast[6] = e;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) sm.bcast[7] = 0;
+}
+
+// Bin of a score on a linear scale over [smin, smin + 2048 / scale]; the
+// rounded steps are non-decreasing in s (no contraction), so a larger score
+// never lands in a lower bin and equal scores share a bin.
+__device__ __forceinline__ int value_bin(float s, float smin, float scale) {
+  return min(kBins - 1, __float2int_rz(__fmul_rn(__fsub_rn(s, smin), scale)));
+}
+
+// Top-k + spans + gamma decision for sequence b (whole CTA).
+//
+// Threshold: the k-th largest order key K* (with n_gt keys above it and n_eq
+// equal to it). Fast path: a histogram with 2048 bins linear in the score
+// value between the row's minimum and maximum finds the bin holding the k-th
+// score; when it holds at most kCand scores they are gathered and ranked
+// exactly. Otherwise (clustered or tied scores) the search runs over the key
+// space: a window that starts as [min key, max key] narrows, 2048 bins at a
+// time, to the bin holding the k-th key, until that bin holds at most kCand
+// keys (ranked exactly) or a single key value. Equal keys always share a bin,
+// so n_eq counts every key equal to K*. The selection is every key > K* plus
+// the (k - n_gt) lowest-index keys equal to K*.
+__device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int N = seq_blocks(a, b);
   const int kreq = a.k_per_seq[b];
@@ -100,77 +201,128 @@ __device__ void select_sequence(const ScoreArgs& a, int b, uint32_t* keys_s, uin
   const float* sc = a.scores + int64_t(b) * a.max_blocks;
   const int KPT = (N + kThreads - 1) / kThreads;     // keys per thread, index order
   const int c0 = min(N, tid * KPT), c1 = min(N, c0 + KPT);
+  const bool partial = k > 0 && k < N;
+  uint32_t* keys_s = sm.keys;
+  uint8_t* flags_s = sm.flags;
 
-  for (int i = tid; i < N; i += kThreads) keys_s[i] = order_key(__ldcg(sc + i));
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  for (int i = tid; i < N; i += kThreads) {
+    const uint32_t key = order_key(__ldcg(sc + i));
+    keys_s[i] = key;
+    kmin = min(kmin, key);
+    kmax = max(kmax, key);
+  }
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) {
+    sm.mm[warp] = kmin;
+    sm.mm[kWarps + warp] = kmax;
+  }
   __syncthreads();
-
-  // ---- radix select: threshold key K* and how many ties at K* to take ----
-  uint32_t prefix = 0, mask = 0;
-  int k_rem = k;
-  const bool take_all = (k >= N);
-  if (k > 0 && !take_all) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) hist_s[tid] = 0;
-      __syncthreads();
-      for (int i = 0; i < KPT; ++i) {
-        const int idx = c0 + i;
-        const uint32_t key = idx < c1 ? keys_s[idx] : 0u;
-        const bool valid = idx < c1 && (key & mask) == prefix;
-        if (valid) atomicAdd(&hist_s[(key >> shift) & 255u], 1);
-      }
-      __syncthreads();
-      // suffix sums over the 256 bins: warp w < 8 owns bins [32w, 32w + 32)
-      int h = 0, x = 0;
-      if (warp < 8) {
-        h = hist_s[warp * 32 + lane];
-        x = h;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const int y = __shfl_down_sync(0xffffffffu, x, off);
-          if (lane + off < 32) x += y;
-        }
-        if (lane == 0) scratch_s[warp] = x;
-      }
+  for (int w = 0; w < kWarps; ++w) {
+    kmin = min(kmin, sm.mm[w]);
+    kmax = max(kmax, sm.mm[kWarps + w]);
+  }
+
+  uint32_t kstar = 0;
+  int n_gt = 0, n_eq = 0;
+  if (partial && kmin == kmax) {
+    kstar = kmin;                            // one value: take the lowest indices
+    n_eq = N;
+  } else if (partial) {
+    bool done = false;
+    if (N <= kCand) {
+      // few keys: rank them all
+      for (int i = tid; i < N; i += kThreads) sm.cand[i] = keys_s[i];
       __syncthreads();
-      if (warp < 8) {
-        int higher = 0;
-        for (int w = warp + 1; w < 8; ++w) higher += scratch_s[w];
-        const int suffix_incl = x + higher;          // sum_{u >= bin}
-        const int above = suffix_incl - h;           // sum_{u > bin}
-        if (above < k_rem && suffix_incl >= k_rem) {
-          bcast_s[0] = warp * 32 + lane;
-          bcast_s[1] = k_rem - above;
+      rank_candidates(sm, N, k);
+      done = true;
+    } else {
+      const float smin = key_float(kmin), smax = key_float(kmax);
+      const float span = __fsub_rn(smax, smin);
+      const float scale = __fdiv_rn(float(kBins), span);
+      if (isfinite(smin) && isfinite(span) && span > 0.f && isfinite(scale) && scale > 0.f) {
+        for (int i = tid; i < N; i += kThreads)
+          atomicAdd(&sm.hist[value_bin(key_float(keys_s[i]), smin, scale)], 1);
+        __syncthreads();
+        locate_bin(sm, k);
+        const int bin = sm.bcast[0], above = sm.bcast[1], m = sm.bcast[2];
+        if (m <= kCand) {
+          for (int i = tid; i < N; i += kThreads) {
+            const uint32_t key = keys_s[i];
+            if (value_bin(key_float(key), smin, scale) == bin) sm.cand[atomicAdd(&sm.bcast[7], 1)] = key;
+          }
+          __syncthreads();
+          rank_candidates(sm, m, k - above);
+          n_gt = above;
+          done = true;
         }
       }
-      __syncthreads();
-      prefix |= uint32_t(bcast_s[0]) << shift;
-      mask |= 255u << shift;
-      k_rem = bcast_s[1];
+    }
+    if (done) {
+      kstar = uint32_t(sm.bcast[4]);
+      n_gt += sm.bcast[5];
+      n_eq = sm.bcast[6];
+    } else {
+      uint32_t lo = kmin;     // window: lo <= key, (key - lo) < 2^wbits (wbits 32: no upper bound)
+      int wbits = 32;
+      int r = k;              // rank of K* from the top among the window's keys
+      int m = N;              // keys in the window
+      int shift = max(0, (32 - __clz(int(kmax - kmin))) - 11);
+      while (true) {
+        for (int i = tid; i < N; i += kThreads) {
+          const uint32_t key = keys_s[i];
+          const uint32_t dl = key - lo;
+          if (key >= lo && (wbits == 32 || (dl >> wbits) == 0u)) atomicAdd(&sm.hist[dl >> shift], 1);
+        }
+        __syncthreads();
+        locate_bin(sm, r);
+        const int bin = sm.bcast[0];
+        r -= sm.bcast[1];
+        n_gt += sm.bcast[1];
+        m = sm.bcast[2];
+        lo += uint32_t(bin) << shift;
+        wbits = shift;
+        if (shift == 0 || m <= kCand) break;
+        shift = max(0, shift - 11);
+      }
+      if (wbits == 0) {
+        kstar = lo;                          // the bin is one key value
+        n_eq = m;
+      } else {
+        for (int i = tid; i < N; i += kThreads) {
+          const uint32_t key = keys_s[i];
+          if (key >= lo && ((key - lo) >> wbits) == 0u) sm.cand[atomicAdd(&sm.bcast[7], 1)] = key;
+        }
+        __syncthreads();
+        rank_candidates(sm, m, r);
+        kstar = uint32_t(sm.bcast[4]);
+        n_gt += sm.bcast[5];
+        n_eq = sm.bcast[6];
+      }
     }
   }
-  const uint32_t kstar = prefix;
-  const int need_eq = k_rem;
+  const int need_eq = k - n_gt;              // keys equal to K* to take, lowest index first
 
-  // ---- pass A: selection flags in index order (ties -> lower index) ----
-  int eq_cnt = 0;
-  if (k > 0 && !take_all)
+  // ---- selection flags in index order ----
+  if (partial && need_eq < n_eq) {
+    int eq_cnt = 0;
     for (int i = c0; i < c1; ++i) eq_cnt += (keys_s[i] == kstar);
-  int eq_tot;
-  int eq_rank = block_exclusive_scan(eq_cnt, scratch_s, &eq_tot);
-  for (int i = c0; i < c1; ++i) {
-    bool s;
-    if (k == 0) s = false;
-    else if (take_all) s = true;
-    else {
+    int eq_tot;
+    int eq_rank = block_exclusive_scan(eq_cnt, sm.scratch, &eq_tot);
+    for (int i = c0; i < c1; ++i) {
       const uint32_t key = keys_s[i];
-      s = key > kstar;
+      bool s = key > kstar;
       if (key == kstar) { s = eq_rank < need_eq; ++eq_rank; }
+      flags_s[i] = s ? 1 : 0;
     }
-    flags_s[i] = s ? 1 : 0;
+  } else {
+    for (int i = c0; i < c1; ++i) flags_s[i] = (k > 0 && (!partial || keys_s[i] >= kstar)) ? 1 : 0;
   }
   __syncthreads();
 
-  // ---- pass B: positions and span starts (one packed scan), then ends ----
+  // ---- positions and span starts (one packed scan), then span ends ----
   int nsel_c = 0, nstart_c = 0;
   for (int i = c0; i < c1; ++i) {
     if (flags_s[i]) {
@@ -179,7 +331,7 @@ __device__ void select_sequence(const ScoreArgs& a, int b, uint32_t* keys_s, uin
     }
   }
   int packed_tot;
-  const int packed = block_exclusive_scan(nsel_c | (nstart_c << 16), scratch_s, &packed_tot);
+  const int packed = block_exclusive_scan(nsel_c | (nstart_c << 16), sm.scratch, &packed_tot);
   int pos = packed & 0xFFFF, sidx = packed >> 16;
   const int sel_tot = packed_tot & 0xFFFF, start_tot = packed_tot >> 16;
   int32_t* sel_out = a.sel_idx + int64_t(b) * a.k_max;
@@ -212,21 +364,25 @@ __device__ void select_sequence(const ScoreArgs& a, int b, uint32_t* keys_s, uin
 }
 
 template <int VPL>
-__global__ void __launch_bounds__(kThreads, 1) score_topk_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int hist_s[256];
   __shared__ int scratch_s[kWarps];
-  __shared__ int bcast_s[4];
-  __shared__ int last_s[2];
+  // the Top-k grid may be scheduled now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int S = a.stages;
-  unsigned char* stage = smem;                                               // [S][kStageBytes]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(S) * kStageBytes);
+  const int SB = a.stage_bytes;
+  unsigned char* stage = smem;                                               // [S][SB]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(S) * SB);
   float* qf_s = reinterpret_cast<float*>(bars + kMaxStages);                 // Hkv*d floats
   int* base_s = reinterpret_cast<int*>(qf_s + a.Hkv * a.d);                  // batch + 1
-  uint32_t* keys_s = reinterpret_cast<uint32_t*>(base_s + a.batch + 1);      // max_blocks + 2
-  uint8_t* flags_s = reinterpret_cast<uint8_t*>(keys_s + a.max_blocks + 2);  // max_blocks
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+    fence_barrier_init();
+  }
+  // every input may still be being written by an earlier kernel of the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // exclusive prefix of blocks over sequences
   int carry = 0;
   for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
@@ -240,20 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_kernel(ScoreArgs a) {
   if (tid == 0) base_s[a.batch] = carry;
   __syncthreads();
   const int64_t total = carry;
-
-  // sequences with no block never see a ticket: finish them here
-  for (int b = blockIdx.x * kThreads + tid; b < a.batch; b += gridDim.x * kThreads) {
-    if (base_s[b + 1] == base_s[b]) {
-      a.n_sel[b] = 0;
-      a.n_spans[b] = 0;
-      if (a.dense_flag) a.dense_flag[b] = 0;
-      if (a.k_per_seq[b] > a.k_max) latch_error(a.err, KVSEL_ERR_BOUNDS);
-    }
-  }
-  const int64_t g0 = total * blockIdx.x / gridDim.x;
-  const int64_t g1 = total * (blockIdx.x + 1) / gridDim.x;
-  if (g0 >= g1) return;
-
   auto find_seq = [&](int64_t g) {
     int lo = 0, hi = a.batch - 1;
     while (lo < hi) {             // largest b with base_s[b] <= g
@@ -262,12 +404,23 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_kernel(ScoreArgs a) {
     }
     return lo;
   };
-  const int bfirst = find_seq(g0);
-  const int blast = find_seq(g1 - 1);
+  const int CH = a.chunk_blocks;
+  // Equal shares of the flattened (sequence, block) list, each cut moved to
+  // the nearest chunk boundary of its sequence so that copies stay whole.
+  auto cut = [&](int64_t i) -> int64_t {
+    const int64_t g = total * i / gridDim.x;
+    const int b = find_seq(g);
+    const int N = base_s[b + 1] - base_s[b];
+    const int n = int(g - base_s[b]);
+    return base_s[b] + min(N, (n + CH / 2) / CH * CH);
+  };
+  const int64_t g0 = cut(blockIdx.x);
+  const int64_t g1 = blockIdx.x + 1 == gridDim.x ? total : cut(blockIdx.x + 1);
+  if (g0 >= g1) return;
+
   const int NV = a.NV;
   const int block_bytes = NV * 16;
-  const int CH = a.chunk_blocks;
-
+  const uint32_t q_bytes = uint32_t(a.Hq) * a.d * 2;
   // chunks of the range never cross a sequence end or the range end
   auto chunk_at = [&](int64_t g, int& b, int& n0, int& nblk) {
     b = find_seq(g);
@@ -275,23 +428,23 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_kernel(ScoreArgs a) {
     const int64_t seq_end = base_s[b + 1];
     nblk = int(min(int64_t(CH), min(seq_end, g1) - g));
   };
-  if (tid == 0) {
-    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-  // producer (thread 0): the next chunk to copy starts at prod_g
+  // producer (thread 0): the next chunk to copy starts at prod_g; the query
+  // rows of a sequence travel with its first chunk in this CTA
   int64_t prod_g = g0;
   int n_issued = 0;
+  int q_issued_b = -1;
   auto issue_next = [&]() {
     if (prod_g >= g1) return;
     int b, n0, nblk;
     chunk_at(prod_g, b, n0, nblk);
     uint64_t* bar = &bars[n_issued % S];
+    unsigned char* dst = stage + size_t(n_issued % S) * SB;
     const uint32_t bytes = uint32_t(nblk) * block_bytes;
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_load(stage + size_t(n_issued % S) * kStageBytes,
-              a.summaries + (int64_t(b) * a.max_blocks + n0) * NV * 8, bytes, bar);
+    const bool with_q = b != q_issued_b;
+    mbar_arrive_expect_tx(bar, bytes + (with_q ? q_bytes : 0u));
+    bulk_load(dst, a.summaries + (int64_t(b) * a.max_blocks + n0) * NV * 8, bytes, bar);
+    if (with_q) bulk_load(dst + kStageBytes, a.q + int64_t(b) * a.Hq * a.d, q_bytes, bar);
+    q_issued_b = b;
     prod_g += nblk;
     ++n_issued;
   };
@@ -308,11 +461,16 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_kernel(ScoreArgs a) {
   for (int64_t g = g0; g < g1; ++c) {
     int b, n0, nblk;
     chunk_at(g, b, n0, nblk);
+    if (!dead && !mbar_wait_bounded(&bars[c % S], uint32_t((c / S) & 1))) {
+      dead = true;
+      if (tid == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
+    }
+    const unsigned char* st = stage + size_t(c % S) * SB;
     if (b != cur_b) {
+      // fold q over the GQA group, from the query rows that came with this chunk
       cur_b = b;
-      const kvsel_bf16* qb = a.q + int64_t(b) * a.Hq * a.d;
+      const kvsel_bf16* qs = reinterpret_cast<const kvsel_bf16*>(st + kStageBytes);
       if constexpr (VPL <= 4) {
-        // fold q over the GQA group for this lane's vectors, straight from global
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int e0 = (li + LPB * i) * 8;
@@ -320,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_kernel(ScoreArgs a) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) qreg[i][e] = 0.f;
           for (int r = 0; r < G; ++r) {
-            const uint4 v = *reinterpret_cast<const uint4*>(qb + int64_t(j * G + r) * a.d + cc);
+            const uint4 v = *reinterpret_cast<const uint4*>(qs + (j * G + r) * a.d + cc);
             qreg[i][0] += bf16lo(v.x); qreg[i][1] += bf16hi(v.x);
             qreg[i][2] += bf16lo(v.y); qreg[i][3] += bf16hi(v.y);
             qreg[i][4] += bf16lo(v.z); qreg[i][5] += bf16hi(v.z);
@@ -331,19 +489,13 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_kernel(ScoreArgs a) {
         for (int e = tid; e < a.Hkv * a.d; e += kThreads) {
           const int j = e / a.d, cc = e % a.d;
           float acc = 0.f;
-          for (int r = 0; r < G; ++r)
-            acc += __uint_as_float(uint32_t(qb[int64_t(j * G + r) * a.d + cc]) << 16);
+          for (int r = 0; r < G; ++r) acc += __uint_as_float(uint32_t(qs[(j * G + r) * a.d + cc]) << 16);
           qf_s[e] = acc;
         }
         __syncthreads();
       }
     }
-    if (!dead && !mbar_wait_bounded(&bars[c % S], uint32_t((c / S) & 1))) {
-      dead = true;
-      if (tid == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
-    }
     if (!dead) {
-      const unsigned char* st = stage + size_t(c % S) * kStageBytes;
       float* out = a.scores + int64_t(b) * a.max_blocks + n0;
       const int steps = (nblk + BPW - 1) / BPW;
       for (int s = warp; s < steps; s += kWarps) {
@@ -387,35 +539,33 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_kernel(ScoreArgs a) {
   // no copy may land after the CTA exits: drain what a timeout left in flight
   if (dead && tid == 0)
     for (int i = c; i < n_issued; ++i) (void)mbar_wait_bounded(&bars[i % S], uint32_t((i / S) & 1));
+}
 
-  // publish scores, take tickets for the first and last sequence touched
-  __threadfence();
+// One CTA per sequence: Top-k, spans and the gamma decision on the scores the
+// score grid wrote. Launched as a programmatic dependent of that grid.
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(ScoreArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int hist_s[kBins];
+  __shared__ uint32_t cand_s[kCand];
+  __shared__ int scratch_s[kWarps];
+  __shared__ uint32_t mm_s[2 * kWarps];
+  __shared__ int bcast_s[8];
+  // the decode grid may be scheduled now; it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kBins; i += kThreads) hist_s[i] = 0;
+  if (tid < 8) bcast_s[tid] = 0;
+  SelectSmem sel;
+  sel.keys = reinterpret_cast<uint32_t*>(smem);                              // max_blocks + 2
+  sel.flags = reinterpret_cast<uint8_t*>(sel.keys + a.max_blocks + 2);       // max_blocks
+  sel.hist = hist_s;
+  sel.cand = cand_s;
+  sel.scratch = scratch_s;
+  sel.mm = mm_s;
+  sel.bcast = bcast_s;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
-  if (tid == 0) {
-    last_s[0] = last_s[1] = -1;
-    const int cand[2] = {bfirst, blast};
-    for (int cI = 0; cI < 2; ++cI) {
-      const int b = cand[cI];
-      if (cI == 1 && blast == bfirst) break;
-      const int64_t s0 = max(int64_t(g0), int64_t(base_s[b]));
-      const int64_t s1 = min(int64_t(g1), int64_t(base_s[b + 1]));
-      const uint32_t mine = uint32_t(s1 - s0);
-      const uint32_t nb = uint32_t(base_s[b + 1] - base_s[b]);
-      const uint32_t before = atomicAdd(&a.tickets[b], mine);
-      if (before + mine == nb) last_s[cI] = b;
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  // sequences strictly inside the range are owned entirely by this CTA
-  for (int b = bfirst; b <= blast; ++b) {
-    const bool inner = (b != bfirst && b != blast);
-    const bool mine = inner || (b == bfirst && last_s[0] == b) || (b == blast && last_s[1] == b);
-    if (!mine) continue;
-    if (inner && base_s[b + 1] == base_s[b]) continue;
-    select_sequence(a, b, keys_s, flags_s, hist_s, scratch_s, bcast_s);
-    if (tid == 0 && !inner) a.tickets[b] = 0;
-  }
+  select_sequence(a, blockIdx.x, sel);
 }
 
 __global__ void merge_spans_kernel(const int32_t* __restrict__ sel_idx, const int32_t* __restrict__ n_sel,
@@ -450,10 +600,12 @@ __global__ void merge_spans_kernel(const int32_t* __restrict__ sel_idx, const in
 }  // namespace
 
 size_t score_topk_ws_bytes(const kvsel_problem& p) {
-  const size_t tickets = (size_t(p.batch) * 4 + 255) / 256 * 256;
+  // a reserved (zero-filled) word per sequence, then the fp32 score rows
+  const size_t reserved = (size_t(p.batch) * 4 + 255) / 256 * 256;
   const size_t scores = size_t(p.batch) * p.max_blocks * 4;
-  return tickets + scores;
+  return reserved + scores;
 }
+
 
 cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
                               const kvsel_bf16* summaries, const int32_t* seq_lens,
@@ -468,7 +620,6 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
   a.sel_idx = sel_idx; a.n_sel = n_sel; a.span_start = span_start; a.span_len = span_len;
   a.n_spans = n_spans; a.dense_flag = dense_flag;
   char* w = static_cast<char*>(ws);
-  a.tickets = reinterpret_cast<uint32_t*>(w);
   a.scores = scores_out ? scores_out
                         : reinterpret_cast<float*>(w + (size_t(p.batch) * 4 + 255) / 256 * 256);
   a.err = err;
@@ -481,25 +632,31 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
   const int vpl = a.NV / lpb;
   const int block_bytes = a.NV * 16;
   a.chunk_blocks = std::max(1, kStageBytes / block_bytes);
+  const size_t q_bytes = size_t(p.n_qheads) * p.head_dim * 2;
+  a.stage_bytes = int((kStageBytes + q_bytes + 127) / 128 * 128);
+  // after the stages: barriers, folded q, sequence prefix
   const size_t tail = size_t(kMaxStages) * 8 + size_t(p.n_kvheads) * p.head_dim * 4 +
-                      (size_t(p.batch) + 1) * 4 + (size_t(p.max_blocks) + 2) * 4 +
-                      size_t(p.max_blocks) + 256;
+                      (size_t(p.batch) + 1) * 4;
   const int max_optin = max_smem_optin();
-  const int static_smem = 256 * 4 + kWarps * 4 + 32 + 64;
-  int stages = int((int64_t(max_optin) - static_smem - int64_t(tail)) / kStageBytes);
-  stages = std::min(kMaxStages, stages);
+  const size_t static_smem = kWarps * 4 + 256;
+  int stages = 0;
+  for (int st = kMaxStages; st >= 1; --st)
+    if (size_t(st) * a.stage_bytes + tail + static_smem <= size_t(max_optin)) {
+      stages = st;
+      break;
+    }
   if (stages < 1) return cudaErrorInvalidConfiguration;
   a.stages = stages;
-  const size_t smem = size_t(stages) * kStageBytes + tail;
+  const size_t smem = size_t(stages) * a.stage_bytes + tail;
   const int64_t upper = int64_t(p.batch) * p.max_blocks;
   const int grid = int(std::min<int64_t>(sm_count(), std::max<int64_t>(1, upper / 8)));
   cudaError_t e = cudaSuccess;
 #define KVSEL_SCORE_CASE(V)                                                                  \
   case V: {                                                                                  \
-    auto kfn = score_topk_kernel<V>;                                                         \
+    auto kfn = score_kernel<V>;                                                              \
     e = ensure_smem(reinterpret_cast<const void*>(kfn), int(smem));                          \
     if (e != cudaSuccess) return e;                                                          \
-    kfn<<<grid, kThreads, smem, s>>>(a);                                                     \
+    e = launch_pdl(kfn, dim3(grid), dim3(kThreads), smem, s, a);                             \
     break;                                                                                   \
   }
   switch (vpl) {
@@ -513,7 +670,13 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
   }
 #undef KVSEL_SCORE_CASE
   count_launch();
-  return cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t sel_smem = ((size_t(p.max_blocks) + 2) * 4 + size_t(p.max_blocks) + 127) / 128 * 128;
+  e = ensure_smem(reinterpret_cast<const void*>(select_kernel), int(sel_smem));
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(select_kernel, dim3(p.batch), dim3(kThreads), sel_smem, s, a);
+  count_launch();
+  return e;
 }
 
 cudaError_t launch_merge_spans(const kvsel_problem& p, const int32_t* sel_idx,

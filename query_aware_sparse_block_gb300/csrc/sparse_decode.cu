@@ -168,6 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
 
   // the merge kernel may be scheduled now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // every input may still be being written by an earlier kernel of the stream
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int NA = HPG * kWPH;                 // active warps per ring
   const int ring = warp / kRingWarps, task = warp % kRingWarps;
@@ -616,22 +618,12 @@ cudaError_t launch_t(const kvsel_problem& p, const DecodeArgs& a0, cudaStream_t 
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(kfn), int(smem));
   if (e != cudaSuccess) return e;
   const int grid = std::min(kMaxCtas, sm_count());
-  kfn<<<grid, kThreads, smem, s>>>(a);
+  e = launch_pdl(kfn, dim3(grid), dim3(kThreads), smem, s, a);
   count_launch();
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the row merge, as a programmatic dependent of the decode grid
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned((int64_t(p.batch) * p.n_qheads + 3) / 4));
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, merge_rows_kernel<D>, a, int(B / 16));
+  const unsigned merge_grid = unsigned((int64_t(p.batch) * p.n_qheads + 3) / 4);
+  e = launch_pdl(merge_rows_kernel<D>, dim3(merge_grid), dim3(128), 0, s, a, int(B / 16));
   count_launch();
   return e;
 }

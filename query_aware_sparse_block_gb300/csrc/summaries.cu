@@ -58,6 +58,9 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
     const kvsel_bf16* __restrict__ k_pages, int64_t n_pages, const int32_t* __restrict__ block_table,
     const int32_t* __restrict__ seq_lens, kvsel_bf16* __restrict__ summaries,
     double* __restrict__ open_acc, int H, int d, int B, int max_blocks, int* err) {
+  // a kernel launched after this one with programmatic serialization may
+  // become resident now; it waits for this grid's completion before reading
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int n = blockIdx.x;
   const int b = blockIdx.y;
   int T = seq_lens[b];
@@ -124,6 +127,7 @@ __global__ void __launch_bounds__(kThreads) summaries_append_kernel(
     const kvsel_bf16* __restrict__ new_k, const kvsel_bf16* __restrict__ new_v,
     kvsel_bf16* __restrict__ summaries, double* __restrict__ open_acc, int H, int d, int B,
     int max_blocks, int* err) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int b = blockIdx.x;
   const int t = append_pos[b];
   if (t < 0) return;

@@ -1,0 +1,95 @@
+"""Top-k threshold search on scores chosen exactly.
+
+The summaries carry one non-zero channel (KV head 0, channel 0) and the query
+is the unit vector on that channel, so every block score equals a bf16 value
+picked here: heavy ties, all-equal rows, runs of adjacent floating-point
+values (the search must narrow down to a single key value), ties that
+straddle the k-th score, rows short enough to be ranked directly, and rows of
+16384 blocks. Selection, spans and the dense flag must equal the oracle's
+Top-k (ties to the lower index, "SparPR KV cache recovery on a consumer GPU",
+paragraph "Query-Aware key-block selection") bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as o
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def K():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from query_aware_sparse_block_gb300.build import build_library
+    build_library()
+    from query_aware_sparse_block_gb300 import kvsel
+    kvsel.lib()
+    torch.cuda.set_device(0)
+    return kvsel
+
+
+def _rows(rng):
+    adj = (1.0 + rng.integers(0, 128, 5000) / 128.0).astype(np.float32)          # adjacent bf16 values
+    mixed = np.concatenate([rng.standard_normal(1500) * 1e-4, rng.standard_normal(1500) * 1e3])
+    straddle = np.full(3000, -1.0); straddle[:200] = 5.0; straddle[rng.choice(3000, 400, replace=False)] = 2.0
+    return [
+        (rng.integers(-3, 4, 16384).astype(np.float64), 2048),       # 7 distinct values
+        (np.full(16384, 0.75), 100),                                # all equal
+        (adj.astype(np.float64), 777),
+        (rng.standard_normal(3000), 375),
+        (mixed, 300),
+        (straddle, 350),                                            # 200 above, take 150 of 400 tied
+        (rng.integers(0, 3, 100).astype(np.float64), 37),           # short row: direct ranking
+        (np.array([1.5]), 1),
+        (rng.standard_normal(7), 0),
+        (rng.standard_normal(129), 128),
+        (rng.standard_normal(16384), 16383),
+    ]
+
+
+def test_threshold_search_paths_match_oracle(K):
+    rng = np.random.default_rng(42)
+    rows = _rows(rng)
+    batch, Hkv, d, B, max_blocks = len(rows), 1, 64, 16, 16384
+    k_max = 16384
+    dev = torch.device("cuda:0")
+    p = K.problem(batch, 1, Hkv, d, B, max_blocks, k_max)
+    summ = torch.zeros((batch, max_blocks, Hkv, d), dtype=torch.bfloat16)
+    want_vals = []
+    for b, (v, _) in enumerate(rows):
+        vb = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+        summ[b, : len(v), 0, 0] = vb
+        want_vals.append(vb.float().numpy().astype(np.float64))
+    q = torch.zeros((batch, 1, d), dtype=torch.bfloat16)
+    q[:, 0, 0] = 1.0
+    lens = torch.tensor([len(v) * B for v, _ in rows], dtype=torch.int32)
+    ks = torch.tensor([k for _, k in rows], dtype=torch.int32)
+    sel = torch.full((batch, k_max), -1, dtype=torch.int32, device=dev)
+    n_sel = torch.zeros(batch, dtype=torch.int32, device=dev)
+    st = torch.zeros_like(sel); ln = torch.zeros_like(sel)
+    n_sp = torch.zeros_like(n_sel)
+    dense = torch.zeros(batch, dtype=torch.uint8, device=dev)
+    scores = torch.zeros((batch, max_blocks), dtype=torch.float32, device=dev)
+    ws = torch.zeros(K.kvsel_workspace_size(p, K.KVSEL_WS_SCORE_TOPK), dtype=torch.uint8, device=dev)
+    gamma, tau = 0.6, 0.5
+    for _ in range(2):                        # twice: the tickets must come back to zero
+        K.kvsel_score_topk(p, q.to(dev), summ.to(dev), lens.to(dev), ks.to(dev), sel, n_sel, st, ln, n_sp, ws,
+                           gamma=gamma, tau_rel=tau, dense_flag=dense, scores_out=scores)
+        torch.cuda.synchronize()
+        assert K.kvsel_get_error() == 0
+        for b, (v, k) in enumerate(rows):
+            N = len(v)
+            sc = scores[b, :N].cpu().numpy().astype(np.float64)
+            assert np.array_equal(sc, want_vals[b])
+            want = o.topk_blocks(want_vals[b], k)
+            got = sel[b, : int(n_sel[b])].cpu().numpy()
+            assert np.array_equal(got, want), f"row {b}"
+            a_, l_ = o.merge_spans(want)
+            ns = int(n_sp[b])
+            assert ns == len(a_)
+            assert np.array_equal(st[b, :ns].cpu().numpy(), a_) and np.array_equal(ln[b, :ns].cpu().numpy(), l_)
+            assert bool(dense[b]) == o.dense_fallback(len(a_), len(want), N, gamma, tau)
