@@ -150,7 +150,7 @@ class Workbench:
             x = generate_layer(w, l, device=device, max_blocks=self.max_blocks, perm=False,
                                seq_lens=[self.T0] * w.batch)
             summ, acc = self.dec.new_summaries()
-            self.dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
+            self.dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
             g = torch.Generator(device=device)
             g.manual_seed(w.seed(l) + 104729)
             shape = (w.batch, w.n_kvheads, w.head_dim)
@@ -171,7 +171,7 @@ class Workbench:
         from query_aware_sparse_block_gb300.runtime import BoundLayer
         import ctypes
         self.K = K
-        self.bound = [BoundLayer(self.dec, d["x"]["q"], d["x"]["k_pages"], d["x"]["v_pages"],
+        self.bound = [BoundLayer(self.dec, d["x"]["q"], d["x"]["kv_pages"],
                                  d["x"]["block_table"], d["summ"], d["acc"], d["out"], d["lse"],
                                  gamma=w.gamma, new_k=d["new_k"], new_v=d["new_v"])
                       for d in self.layers]
@@ -443,8 +443,8 @@ def oracle_sample_inputs(n_seqs: int):
     x = generate_layer(w, 0, device="cpu", perm=False)
     seqs = []
     for b in range(n_seqs):
-        seqs.append(dict(q=bits(x["q"][b]), k=bits(logical_kv(x["k_pages"], x["block_table"], b, w.seq_len)),
-                         v=bits(logical_kv(x["v_pages"], x["block_table"], b, w.seq_len))))
+        seqs.append(dict(q=bits(x["q"][b]), k=bits(logical_kv(x["kv_pages"], x["block_table"], b, w.seq_len, 0)),
+                         v=bits(logical_kv(x["kv_pages"], x["block_table"], b, w.seq_len, 1))))
     return w, seqs
 
 

@@ -34,28 +34,29 @@
  *
  * Layouts (row-major, innermost last)
  *  q            [batch][n_qheads][head_dim]                    bf16
- *  K / V pages  [n_pages][n_kvheads][head_dim/64][block_size][64] bf16,
- *               "tiled": each (page, KV head) tile keeps its block_size x
- *               head_dim keys as head_dim/64 column halves of block_size rows
- *               x 64 channels, and inside every 128-byte row the 16-byte chunk
- *               c of token row t is stored at chunk position c ^ (t % 8). A
- *               tile is therefore one contiguous range, and so is a run of
- *               consecutive heads of a page.
+ *  KV pages     [n_pages][n_kvheads][2][head_dim/64][block_size][64] bf16:
+ *               for each (page, KV head) the K tile, then the V tile. A tile
+ *               is "tiled": it keeps its block_size x head_dim values as
+ *               head_dim/64 column halves of block_size rows x 64 channels,
+ *               and inside every 128-byte row the 16-byte chunk c of token row
+ *               t is stored at chunk position c ^ (t % 8). The K and V of a
+ *               run of consecutive heads of a page are one contiguous range.
  *  block_table  [batch][max_blocks]                            int32 (page id)
  *  seq_lens     [batch]                                        int32 (T_b)
  *  summaries    [batch][max_blocks][n_kvheads][head_dim]       bf16
  *  open_acc     [batch][n_kvheads][head_dim]                   fp64
  *  sel_idx      [batch][k_max]  ascending block indices        int32
  *  spans        span_start / span_len [batch][k_max]           int32
- *  host tier    [batch][host_blocks][2][one page of K or V] bf16, tiled as the
- *               pages (K then V of one block contiguous, spans contiguous)
- *  staging      [batch][staging_slots][2][one page of K or V] bf16, tiled
+ *  host tier    [batch][host_blocks][one KV page] bf16 (block n of sequence
+ *               b is a copy of its page, so spans are contiguous)
+ *  staging      [batch][staging_slots][one KV page] bf16
  *  out          [batch][n_qheads][head_dim] fp32; lse [batch][n_qheads] fp32
  * A sequence b holds T_b = seq_lens[b] tokens in N_b = ceil(T_b / block_size)
  * blocks; token t lives in page block_table[b][t / block_size], row
- * t % block_size. Channel c of token row t of KV head j of page p is element
- * ((p * n_kvheads + j) * head_dim/64 + c/64) * block_size * 64 + t * 64 +
- * (((c % 64) / 8) ^ (t % 8)) * 8 + c % 8.
+ * t % block_size. Channel c of token row t of the key (v = 0) or value
+ * (v = 1) of KV head j in page p is element
+ * (((p * n_kvheads + j) * 2 + v) * head_dim/64 + c/64) * block_size * 64 +
+ * t * 64 + (((c % 64) / 8) ^ (t % 8)) * 8 + c % 8.
  */
 #ifndef KVSEL_H_
 #define KVSEL_H_
@@ -122,7 +123,7 @@ enum kvsel_summary_mode {
  *         summary of block t / B is rewritten from it over t % B + 1 tokens.
  *         The caller sets seq_lens[b] = t + 1 for the steps that follow.
  *
- * k_pages, v_pages: paged cache (v_pages only written by APPEND with new_v).
+ * kv_pages: the paged cache (written only by APPEND with new_k / new_v).
  * block_table, seq_lens: device int32. append_pos: device [batch] int32.
  * new_k, new_v: device [batch][n_kvheads][head_dim] bf16 in natural channel
  * order, nullable; they are stored into the tiled page layout.
@@ -131,11 +132,12 @@ enum kvsel_summary_mode {
  * device BOUNDS when a block-table entry is negative or >= n_pages or
  * T_b > max_blocks * B (the access is skipped).
  */
-KVSEL_API int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16* k_pages,
-                          kvsel_bf16* v_pages, int64_t n_pages, const int32_t* block_table,
-                          const int32_t* seq_lens, const int32_t* append_pos,
-                          const kvsel_bf16* new_k, const kvsel_bf16* new_v,
-                          kvsel_bf16* summaries, double* open_acc, kvsel_stream_t stream);
+KVSEL_API int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16* kv_pages,
+                                    int64_t n_pages, const int32_t* block_table,
+                                    const int32_t* seq_lens, const int32_t* append_pos,
+                                    const kvsel_bf16* new_k, const kvsel_bf16* new_v,
+                                    kvsel_bf16* summaries, double* open_acc,
+                                    kvsel_stream_t stream);
 
 /*
  * kvsel_score_topk -- query-aware block score, Top-k and span merge
@@ -221,10 +223,9 @@ enum kvsel_kv_kind {
 typedef struct kvsel_kv_src {
   int32_t kind;                   /* enum kvsel_kv_kind */
   int32_t staging_slots;          /* STAGED/HOST: block slots per sequence in staging */
-  const kvsel_bf16* k_pages;      /* PAGED */
-  const kvsel_bf16* v_pages;      /* PAGED */
+  const kvsel_bf16* kv_pages;     /* PAGED */
   const int32_t* block_table;     /* PAGED */
-  int64_t n_pages;                /* PAGED: pages in k_pages and v_pages */
+  int64_t n_pages;                /* PAGED: pages in kv_pages */
   kvsel_bf16* staging;            /* STAGED/HOST: device staging buffer */
   const kvsel_bf16* host_kv;      /* HOST: pinned host tier (device-mapped) */
   int32_t host_blocks;            /* HOST: block stride of the host tier per sequence */

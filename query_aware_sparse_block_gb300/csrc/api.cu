@@ -212,35 +212,36 @@ int kvsel_get_error(kvsel_stream_t stream) {
   return h;
 }
 
-int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16* k_pages,
-                          kvsel_bf16* v_pages, int64_t n_pages, const int32_t* block_table,
-                          const int32_t* seq_lens, const int32_t* append_pos,
-                          const kvsel_bf16* new_k, const kvsel_bf16* new_v,
-                          kvsel_bf16* summaries, double* open_acc, kvsel_stream_t stream) {
+int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16* kv_pages, int64_t n_pages,
+                          const int32_t* block_table, const int32_t* seq_lens,
+                          const int32_t* append_pos, const kvsel_bf16* new_k,
+                          const kvsel_bf16* new_v, kvsel_bf16* summaries, double* open_acc,
+                          kvsel_stream_t stream) {
   int r = check_problem(p);
   if (r) return r;
   if (mode != KVSEL_SUMMARY_FULL && mode != KVSEL_SUMMARY_APPEND)
     return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: mode must be FULL or APPEND");
   if (p->batch == 0) return KVSEL_OK;
-  if (!k_pages || !block_table || !summaries || !open_acc || n_pages <= 0)
+  if (!kv_pages || !block_table || !summaries || !open_acc || n_pages <= 0)
     return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: NULL pointer or no pages");
-  if (!aligned16(k_pages) || !aligned16(summaries) || !aligned16(open_acc) ||
-      !aligned4(block_table) || (v_pages && !aligned16(v_pages)))
+  if (!aligned16(kv_pages) || !aligned16(summaries) || !aligned16(open_acc) || !aligned4(block_table))
     return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: misaligned pointer");
+  if (n_pages * p->n_kvheads * 2 * p->block_size >= (int64_t(1) << 31))
+    return fail(KVSEL_ERR_UNSUPPORTED, "build_summaries: more than 2^31 cache rows");
   if (mode == KVSEL_SUMMARY_FULL && !seq_lens)
     return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: FULL needs seq_lens");
   if (mode == KVSEL_SUMMARY_APPEND) {
     if (!append_pos) return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: APPEND needs append_pos");
     if ((new_k && !aligned16(new_k)) || (new_v && !aligned16(new_v)))
       return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: misaligned new_k/new_v");
-    if (new_v && (!new_k || !v_pages))
-      return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: new_v needs new_k and v_pages");
+    if (new_v && !new_k)
+      return fail(KVSEL_ERR_INVALID_ARG, "build_summaries: new_v needs new_k");
   }
   int* ew = device_error_word();
   if (!ew) return fail(KVSEL_ERR_CUDA, "build_summaries: no CUDA device");
-  return cuda_status(launch_build_summaries(*p, mode, k_pages, v_pages, n_pages, block_table,
-                                            seq_lens, append_pos, new_k, new_v, summaries,
-                                            open_acc, ew, reinterpret_cast<cudaStream_t>(stream)),
+  return cuda_status(launch_build_summaries(*p, mode, kv_pages, n_pages, block_table, seq_lens,
+                                            append_pos, new_k, new_v, summaries, open_acc, ew,
+                                            reinterpret_cast<cudaStream_t>(stream)),
                      "build_summaries launch");
 }
 
@@ -299,7 +300,7 @@ static int check_host_kv(const kvsel_problem* p, const kvsel_kv_src* kv, const v
   if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr)
     return fail(KVSEL_ERR_INVALID_ARG, "host tier: host_kv is not device-mapped pinned memory");
   *dev_ptr = at.devicePointer;
-  const int64_t rows = int64_t(p->batch) * kv->staging_slots * 2 * p->n_kvheads * p->block_size;
+  const int64_t rows = int64_t(p->batch) * kv->staging_slots * p->n_kvheads * 2 * p->block_size;
   if (rows >= (int64_t(1) << 31))
     return fail(KVSEL_ERR_UNSUPPORTED, "host tier: staging larger than 2^31 rows");
   return KVSEL_OK;
@@ -352,11 +353,11 @@ int kvsel_sparse_decode(const kvsel_problem* p, const kvsel_bf16* q, const kvsel
   if (!ew) return fail(KVSEL_ERR_CUDA, "sparse_decode: no CUDA device");
   kvsel_kv_src src = *kv;
   if (kv->kind == KVSEL_KV_PAGED) {
-    if (!kv->k_pages || !kv->v_pages || !kv->block_table || kv->n_pages <= 0)
+    if (!kv->kv_pages || !kv->block_table || kv->n_pages <= 0)
       return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: paged source needs pages and a block table");
-    if (!aligned16(kv->k_pages) || !aligned16(kv->v_pages))
+    if (!aligned16(kv->kv_pages))
       return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: misaligned pages");
-    if (kv->n_pages * p->n_kvheads * p->block_size >= (int64_t(1) << 31))
+    if (kv->n_pages * p->n_kvheads * 2 * p->block_size >= (int64_t(1) << 31))
       return fail(KVSEL_ERR_UNSUPPORTED, "sparse_decode: more than 2^31 cache rows");
   } else if (kv->kind == KVSEL_KV_STAGED || kv->kind == KVSEL_KV_HOST) {
     if (kv->kind == KVSEL_KV_HOST) {

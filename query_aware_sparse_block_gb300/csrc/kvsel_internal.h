@@ -22,8 +22,8 @@ cudaError_t ensure_smem(const void* kernel, int bytes);
 void set_last_error(const char* fmt, ...);
 
 // ---- summaries (summaries.cu) ----
-cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16* k_pages,
-                                   kvsel_bf16* v_pages, int64_t n_pages, const int32_t* block_table,
+cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16* kv_pages,
+                                   int64_t n_pages, const int32_t* block_table,
                                    const int32_t* seq_lens, const int32_t* append_pos,
                                    const kvsel_bf16* new_k, const kvsel_bf16* new_v,
                                    kvsel_bf16* summaries, double* open_acc, int* err,

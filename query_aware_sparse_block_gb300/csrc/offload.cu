@@ -7,8 +7,8 @@
 //
 // The gather kernel copies, for every sequence, the blocks of its spans (or
 // all blocks when the dense fallback fired) from the host tier
-// [b][host_blocks][2][H_kv][B][d] into consecutive staging slots
-// [b][slots][2][H_kv][B][d]. Each CTA owns one sequence row of the grid and a
+// [b][host_blocks][one KV page] into consecutive staging slots
+// [b][slots][one KV page]; a page is copied opaquely. Each CTA owns one sequence row of the grid and a
 // share of that sequence's blocks; within a block the CTA streams 16-byte
 // host reads with several requests in flight per thread. The span list never
 // leaves the GPU, so there is no host round trip between selection and fetch.

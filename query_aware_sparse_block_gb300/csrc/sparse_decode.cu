@@ -7,13 +7,13 @@
 // Design (GB300):
 //  * Work unit: a tile is one attended block of one sequence for a group of
 //    HPG consecutive KV heads. The selection is per sequence, so all heads of
-//    a page are needed, and a page stores its heads contiguously in the tiled
-//    layout: the tile's K is one contiguous range, its V another. Two 1-D bulk
-//    (TMA) copies move them into shared memory unchanged; HPG is chosen so
-//    that each is 16 KiB for d = 128, which keeps DRAM bursts long (scattered
-//    bulk copies of >= 16 KiB stream near the HBM read peak, tensor-map boxes
-//    of 128-byte rows do not). The tiled layout already carries the 16-byte chunk swizzle
-//    (chunk c of row t at c ^ (t % 8)), so ldmatrix reads are conflict-free.
+//    a page are needed, and a page stores each head's K tile and V tile next
+//    to each other, heads in order: a tile's K and V are one contiguous range
+//    (32 KiB for d = 128 and HPG * B = 64 rows), moved into shared memory by a
+//    single 1-D bulk (TMA) copy. Scattered 32 KiB copies stream markedly
+//    faster than pairs of 16 KiB ones on GB300 HBM3e. The tiled layout already
+//    carries the 16-byte chunk swizzle (chunk c of row t at c ^ (t % 8)), so
+//    ldmatrix reads are conflict-free.
 //  * Work list: the flattened (sequence, head group, block) tiles are split
 //    into equal contiguous ranges, one per CTA (one CTA per SM), so the HBM
 //    stream is balanced whatever the per-sequence selection sizes are. At the
@@ -28,14 +28,17 @@
 //    slot (a shared-memory counter) refills it, so no warp waits on another
 //    and the two rings drift apart instead of hitting the tensor pipe in
 //    lockstep.
-//  * Math: the GQA group's query heads (G <= 16, zero-padded to 16 rows) form
-//    the A operand of mma.m16n8k16 bf16 tensor-core tiles: S = Q K^T with K
-//    read by ldmatrix from the swizzled tile, online softmax in fp32 (exp2 of
-//    log2-scaled logits, accumulators rescaled only when a row max moves),
-//    then O += P V with V read by ldmatrix.trans; P is split into bf16 high
-//    and low parts so the product keeps ~16 bits.
+//  * Math: tokens are the M dimension of mma.m16n8k16 bf16 tensor-core tiles:
+//    S^T = K Q^T with K read by ldmatrix from the swizzled tile and the GQA
+//    group's query heads (G <= 16, zero-padded to 8 or 16 columns) as N, online
+//    softmax in fp32 per head column (exp2 of log2-scaled logits, accumulators
+//    rescaled only when a running max moves), then O^T += V^T P^T with V read
+//    by ldmatrix.trans and P transposed into B fragments by movmatrix; P is
+//    split into bf16 high and low parts so the product keeps ~16 bits.
 //  * Every wait on a copy is bounded; a wait that runs out latches
 //    KVSEL_ERR_TIMEOUT and the warp stops issuing work.
+#include <type_traits>
+
 #include "kvsel_common.cuh"
 #include "kvsel_internal.h"
 
@@ -59,8 +62,7 @@ inline int heads_per_group(int B, int Hkv) {
 }
 
 struct DecodeArgs {
-  const kvsel_bf16* k_base;   // PAGED: K pages; STAGED: staging
-  const kvsel_bf16* v_base;   // PAGED: V pages
+  const kvsel_bf16* kv_base;  // PAGED: KV pages; STAGED: staging (the same page layout)
   const kvsel_bf16* q;
   const int32_t* seq_lens;
   const int32_t* sel_idx;
@@ -74,7 +76,7 @@ struct DecodeArgs {
   float* out;
   kvsel_bf16* out_bf16;
   float* lse;
-  float* partials;     // warp states: [(cta + segment) * W + warp][G][D + 2]
+  float* partials;     // warp states: [(cta + segment) * W + warp][G][D + 4] (m, l, -, -, O)
   int* meta;           // [0] total tiles, [1] active CTAs, [2 ..] tile prefix per sequence
   int* err;
   int batch, Hq, Hkv, G, B, max_blocks, k_max;
@@ -102,7 +104,7 @@ __device__ __forceinline__ int find_seq(const int* base_s, int batch, int64_t g)
   return lo;
 }
 
-// Copy unit of tile g (the K head-group tile's index in units of HPG*B*d
+// Copy unit of tile g (the head group's K+V range, in units of 2*HPG*B*d
 // elements) and its valid token count (0 when the tile is skipped).
 __device__ void tile_info(const DecodeArgs& a, const int* base_s, const int* tlen_s, int64_t g,
                           bool report, int& unit, int& cnt) {
@@ -124,7 +126,7 @@ __device__ void tile_info(const DecodeArgs& a, const int* base_s, const int* tle
   } else {
     int64_t slot = o;
     if (slot >= a.slots) { ok = false; slot = 0; }
-    unit = int((int64_t(b) * a.slots + slot) * 2 * a.n_groups + hg);
+    unit = int((int64_t(b) * a.slots + slot) * a.n_groups + hg);
   }
   if (!ok) {
     cnt = 0;
@@ -132,15 +134,14 @@ __device__ void tile_info(const DecodeArgs& a, const int* base_s, const int* tle
   }
 }
 
-// Shared address of (plane, head h of the group, token row, channel c with
-// c % 8 == 0) in a stage holding the tiled K and V head-group tiles:
-// [plane][head][d/64][row][64], 16-byte chunk c of row t at c ^ (t % 8).
-__device__ __forceinline__ uint32_t swz(uint32_t stage, int plane_bytes, int plane, int h,
-                                        int halves, int B, int row, int c) {
+// Shared address of (head h of the group, kv = 0 for K / 1 for V, token row,
+// channel c with c % 8 == 0) in a slot holding the tile as the page stores it:
+// [head][K, V][d/64][row][64], 16-byte chunk c of row t at c ^ (t % 8).
+__device__ __forceinline__ uint32_t swz(uint32_t stage, int h, int kv, int halves, int B, int row,
+                                        int c) {
   const int half = c >> 6;
   const int chunk = (c & 63) >> 3;
-  return stage + uint32_t(plane * plane_bytes) +
-         uint32_t(((h * halves + half) * B + row) * 128 + ((chunk ^ (row & 7)) << 4));
+  return stage + uint32_t((((h * 2 + kv) * halves + half) * B + row) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
 template <int D, int B, int NTH>
@@ -283,11 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
     uint64_t* bar = slot_bar(m);
     mbar_arrive_expect_tx(bar, uint32_t(tile_bytes));
     unsigned char* dst = tiles + size_t(slot_idx(m)) * tile_bytes;
-    const kvsel_bf16* ksrc = a.k_base + int64_t(unit) * plane_elems;
-    const kvsel_bf16* vsrc = a.kind == KVSEL_KV_PAGED ? a.v_base + int64_t(unit) * plane_elems
-                                                        : ksrc + int64_t(a.n_groups) * plane_elems;
-    bulk_load(dst, ksrc, uint32_t(plane_bytes), bar);
-    bulk_load(dst + plane_bytes, vsrc, uint32_t(plane_bytes), bar);
+    bulk_load(dst, a.kv_base + int64_t(unit) * 2 * plane_elems, uint32_t(tile_bytes), bar);
   };
   if (active) {
     load_batch(0, cur_rk, cur_cnt);
@@ -364,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
             for (int idx = lane; idx < (16 - cnt) * (D / 8); idx += 32) {
               const int row = r0 + cnt + idx / (D / 8);
               const int c = (idx % (D / 8)) * 8;
-              const uint32_t ad = swz(st, plane_bytes, 1, h_local, kHalves, B, row, c);
+              const uint32_t ad = swz(st, h_local, 1, kHalves, B, row, c);
               asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(ad), "r"(0u) : "memory");
             }
             __syncwarp();
@@ -382,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
 #pragma unroll
             for (int ks = 0; ks < kKS; ++ks) {
               uint32_t ka[4];
-              ldsm_x4(swz(st, plane_bytes, 0, h_local, kHalves, B, row, ks * 16 + cofs), ka[0], ka[1],
+              ldsm_x4(swz(st, h_local, 0, kHalves, B, row, ks * 16 + cofs), ka[0], ka[1],
                       ka[2], ka[3]);
 #pragma unroll
               for (int n = 0; n < NTH; ++n) {
@@ -464,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
               uint32_t va[2][4];
 #pragma unroll
               for (int u = 0; u < 2; ++u)
-                ldsm_x4_t(swz(st, plane_bytes, 1, h_local, kHalves, B, row, (mt + u) * 16 + cofs),
+                ldsm_x4_t(swz(st, h_local, 1, kHalves, B, row, (mt + u) * 16 + cofs),
                           va[u][0], va[u][1], va[u][2], va[u][3]);
 #pragma unroll
               for (int u = 0; u < 2; ++u)
@@ -506,22 +503,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
         for (int off = 4; off < 32; off <<= 1) lh[n][c] += __shfl_xor_sync(0xffffffffu, lh[n][c], off);
     if (active) {
       const int64_t seg = int64_t(b) * a.n_groups + hg;
-      float* mw = a.partials + ((int64_t(blockIdx.x) + seg) * kW + warp) * G * (D + 2);
+      float* mw = a.partials + ((int64_t(blockIdx.x) + seg) * kW + warp) * G * (D + 4);
 #pragma unroll
       for (int n = 0; n < NTH; ++n)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int hq = n * 8 + 2 * tq + c;
           if (hq < G) {
-            float* dst = mw + hq * (D + 2);
+            float* dst = mw + hq * (D + 4);
             if (gq == 0) {
               dst[0] = mh[n][c];
               dst[1] = lh[n][c];
             }
 #pragma unroll
             for (int mt = 0; mt < kMT; ++mt) {
-              dst[2 + mt * 16 + gq] = o[mt][n][c];
-              dst[2 + mt * 16 + gq + 8] = o[mt][n][c + 2];
+              dst[4 + mt * 16 + gq] = o[mt][n][c];
+              dst[4 + mt * 16 + gq + 8] = o[mt][n][c + 2];
             }
           }
         }
@@ -536,19 +533,25 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
 }
 
 // One warp per output row (sequence b, query head h): log-sum-exp merge of the
-// states every warp stored for the row's segment. Launched as a programmatic
-// dependent of the decode kernel: it can be resident early and waits for the
-// decode grid's completion before it reads anything that grid wrote.
+// states every warp stored for the row's segment. Lane l owns channels
+// [l * D/32, (l + 1) * D/32); up to 16 states are read at once, every lane
+// loading each state's (max, sum) and its own channel slice, so a chunk of
+// states costs one round trip to L2. Launched as a programmatic dependent of
+// the decode kernel: it can be resident early and waits for the decode grid's
+// completion before it reads anything that grid wrote.
 template <int D>
 __global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a, int wph) {
+  constexpr int kCPL = D / 32;            // channels per lane
+  constexpr int kChunk = 16;              // states in flight per lane
+  using vec_t = typename std::conditional<kCPL == 4, float4, float2>::type;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (row >= int64_t(a.batch) * a.Hq) return;
   const int b = int(row / a.Hq), hq = int(row % a.Hq);
   const int* base = a.meta + 2;
-  const int64_t total = a.meta[0];
-  const int A = a.meta[1];
+  const int64_t total = __ldcg(a.meta);
+  const int A = __ldcg(a.meta + 1);
   const int t0 = __ldcg(base + b), t1 = __ldcg(base + b + 1);
   if (t1 == t0) return;                   // no attended token: written by the decode kernel
   const int G = a.G, j = hq / G, r = hq % G;
@@ -563,43 +566,63 @@ __global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a, int wph) 
   auto state = [&](int i) -> const float* {
     const int c = first_c + i / per_cta, k = i % per_cta;
     const int w = (k / wph) * kRingWarps + h_local * wph + (k % wph);
-    return a.partials + (((int64_t(c) + seg) * kW + w) * G + r) * (D + 2);
+    return a.partials + (((int64_t(c) + seg) * kW + w) * G + r) * (D + 4);
   };
-  float mloc = -INFINITY;
-  for (int i = lane; i < NP; i += 32) mloc = fmaxf(mloc, __ldcg(state(i)));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-  const float ms = mloc;
-  float lloc = 0.f;
-  if (ms != -INFINITY)
-    for (int i = lane; i < NP; i += 32) {
-      const float* st = state(i);
-      lloc += __ldcg(st + 1) * ex2(__ldcg(st) - ms);
-    }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
-  constexpr int kCPL = D / 32;            // channels per lane
+  float M = -INFINITY, L = 0.f;           // running max and sum (log2 domain)
   float acc[kCPL];
 #pragma unroll
   for (int u = 0; u < kCPL; ++u) acc[u] = 0.f;
-  if (ms != -INFINITY) {
-#pragma unroll 4
-    for (int i = 0; i < NP; ++i) {
-      const float* st = state(i);
-      const float f = ex2(__ldcg(st) - ms);
+  for (int i0 = 0; i0 < NP; i0 += kChunk) {
+    float mi[kChunk], li[kChunk];
+    vec_t oi[kChunk];
 #pragma unroll
-      for (int u = 0; u < kCPL; ++u) acc[u] += f * __ldcg(st + 2 + lane * kCPL + u);
+    for (int k = 0; k < kChunk; ++k) {
+      mi[k] = -INFINITY;
+      li[k] = 0.f;
+      if (i0 + k < NP) {
+        const float* st = state(i0 + k);
+        mi[k] = __ldcg(st);
+        li[k] = __ldcg(st + 1);
+        oi[k] = __ldcg(reinterpret_cast<const vec_t*>(st + 4) + lane);
+      }
     }
-  }
-  const float l = lloc;
+    float mc = M;
 #pragma unroll
-  for (int u = 0; u < kCPL; ++u) {
-    const int c = lane * kCPL + u;
-    const float v = l > 0.f ? acc[u] / l : 0.f;
-    a.out[row * D + c] = v;
-    if (a.out_bf16) a.out_bf16[row * D + c] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    for (int k = 0; k < kChunk; ++k) mc = fmaxf(mc, mi[k]);
+    if (mc == -INFINITY) continue;
+    const float rs = M == -INFINITY ? 0.f : ex2(M - mc);
+    L *= rs;
+#pragma unroll
+    for (int u = 0; u < kCPL; ++u) acc[u] *= rs;
+#pragma unroll
+    for (int k = 0; k < kChunk; ++k) {
+      if (i0 + k < NP && mi[k] != -INFINITY) {
+        const float wk = ex2(mi[k] - mc);
+        L += wk * li[k];
+        const float* ov = reinterpret_cast<const float*>(&oi[k]);
+#pragma unroll
+        for (int u = 0; u < kCPL; ++u) acc[u] += wk * ov[u];
+      }
+    }
+    M = mc;
   }
-  if (lane == 0) a.lse[row] = l > 0.f ? (ms + lg2(l)) * 0.6931471805599453f : -INFINITY;
+  vec_t res;
+  float* rv = reinterpret_cast<float*>(&res);
+#pragma unroll
+  for (int u = 0; u < kCPL; ++u) rv[u] = L > 0.f ? acc[u] / L : 0.f;
+  reinterpret_cast<vec_t*>(a.out + row * D)[lane] = res;
+  if (a.out_bf16) {
+    uint32_t pk[kCPL / 2];
+#pragma unroll
+    for (int u = 0; u < kCPL / 2; ++u)
+      pk[u] = uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(rv[2 * u]))) |
+              (uint32_t(__bfloat16_as_ushort(__float2bfloat16_rn(rv[2 * u + 1]))) << 16);
+    if constexpr (kCPL == 4)
+      reinterpret_cast<uint2*>(a.out_bf16 + row * D)[lane] = make_uint2(pk[0], pk[1]);
+    else
+      reinterpret_cast<uint32_t*>(a.out_bf16 + row * D)[lane] = pk[0];
+  }
+  if (lane == 0) a.lse[row] = L > 0.f ? (M + lg2(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 template <int D, int B, int NTH>
@@ -638,7 +661,7 @@ size_t sparse_decode_ws_bytes(const kvsel_problem& p) {
   const int G = p.n_qheads / std::max(1, p.n_kvheads);
   const int hpg = heads_per_group(p.block_size, p.n_kvheads);
   const size_t segments = size_t(p.batch) * (p.n_kvheads / hpg);
-  const size_t parts = (size_t(kMaxCtas) + segments) * kW * G * (p.head_dim + 2) * 4;
+  const size_t parts = (size_t(kMaxCtas) + segments) * kW * G * (p.head_dim + 4) * 4;
   return decode_meta_bytes(p) + parts;
 }
 
@@ -665,13 +688,7 @@ cudaError_t launch_sparse_decode(const kvsel_problem& p, const kvsel_bf16* q,
   a.batch = p.batch; a.Hq = p.n_qheads; a.Hkv = p.n_kvheads; a.G = p.n_qheads / p.n_kvheads;
   a.B = p.block_size; a.max_blocks = p.max_blocks; a.k_max = p.k_max;
   const int D = p.head_dim;
-  if (a.kind == KVSEL_KV_PAGED) {
-    a.k_base = kv.k_pages;
-    a.v_base = kv.v_pages;
-  } else {
-    a.k_base = kv.staging;
-    a.v_base = nullptr;
-  }
+  a.kv_base = a.kind == KVSEL_KV_PAGED ? kv.kv_pages : kv.staging;
   const int Bs = p.block_size;
   if (D == 128 && Bs == 16) return a.G <= 8 ? launch_t<128, 16, 1>(p, a, s) : launch_t<128, 16, 2>(p, a, s);
   if (D == 128 && Bs == 32) return a.G <= 8 ? launch_t<128, 32, 1>(p, a, s) : launch_t<128, 32, 2>(p, a, s);

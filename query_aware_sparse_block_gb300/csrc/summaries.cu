@@ -19,8 +19,10 @@ namespace {
 
 constexpr int kThreads = 128;
 
-// Element offset, inside one (page, head) tile of the tiled layout, of the
-// 8-channel vector starting at channel c0 (c0 % 8 == 0) of token row t.
+// Element offset, inside one K (or V) tile of a (page, head) in the tiled
+// layout, of the 8-channel vector starting at channel c0 (c0 % 8 == 0) of
+// token row t. The page of head j holds the K tile at element (page * H + j)
+// * 2 * B * d and the V tile right after it.
 __device__ __forceinline__ int64_t tiled_off(int t, int c0, int B) {
   const int half = c0 >> 6, chunk = (c0 & 63) >> 3;
   return (int64_t(half) * B + t) * 64 + ((chunk ^ (t & 7)) << 3);
@@ -55,7 +57,7 @@ __device__ __forceinline__ uint4 mean_to_bf16x8(const double (&acc)[8], int cnt)
 // One CTA per (block n, sequence b). Threads own 8-channel column vectors of
 // one KV head and walk the block's tokens in order (pages in the tiled layout).
 __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
-    const kvsel_bf16* __restrict__ k_pages, int64_t n_pages, const int32_t* __restrict__ block_table,
+    const kvsel_bf16* __restrict__ kv_pages, int64_t n_pages, const int32_t* __restrict__ block_table,
     const int32_t* __restrict__ seq_lens, kvsel_bf16* __restrict__ summaries,
     double* __restrict__ open_acc, int H, int d, int B, int max_blocks, int* err) {
   // a kernel launched after this one with programmatic serialization may
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
   for (int v = threadIdx.x; v < n_vec; v += blockDim.x) {
     const int j = v / vec_per_head;
     const int c0 = (v % vec_per_head) * 8;
-    const kvsel_bf16* tile = k_pages + (page * H + j) * int64_t(B) * d;
+    const kvsel_bf16* tile = kv_pages + (page * H + j) * 2 * int64_t(B) * d;
     double acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0;
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
 // One CTA per sequence: write the new token (optional), fold it into the open
 // block's fp64 accumulator and rewrite that block's summary.
 __global__ void __launch_bounds__(kThreads) summaries_append_kernel(
-    kvsel_bf16* __restrict__ k_pages, kvsel_bf16* __restrict__ v_pages, int64_t n_pages,
+    kvsel_bf16* __restrict__ kv_pages, int64_t n_pages,
     const int32_t* __restrict__ block_table, const int32_t* __restrict__ append_pos,
     const kvsel_bf16* __restrict__ new_k, const kvsel_bf16* __restrict__ new_v,
     kvsel_bf16* __restrict__ summaries, double* __restrict__ open_acc, int H, int d, int B,
@@ -147,17 +149,17 @@ __global__ void __launch_bounds__(kThreads) summaries_append_kernel(
   for (int v = threadIdx.x; v < n_vec; v += blockDim.x) {
     const int j = v / vec_per_head;
     const int c0 = (v % vec_per_head) * 8;
-    const int64_t cache_off = (page * H + j) * int64_t(B) * d + tiled_off(row, c0, B);
+    const int64_t k_off = (page * H + j) * 2 * int64_t(B) * d + tiled_off(row, c0, B);
+    const int64_t v_off = k_off + int64_t(B) * d;
     const int64_t tok_off = (int64_t(b) * H + j) * d + c0;
     uint4 kv;
     if (new_k) {
       kv = *reinterpret_cast<const uint4*>(new_k + tok_off);
-      *reinterpret_cast<uint4*>(k_pages + cache_off) = kv;
-      if (new_v && v_pages)
-        *reinterpret_cast<uint4*>(v_pages + cache_off) =
-            *reinterpret_cast<const uint4*>(new_v + tok_off);
+      *reinterpret_cast<uint4*>(kv_pages + k_off) = kv;
+      if (new_v)
+        *reinterpret_cast<uint4*>(kv_pages + v_off) = *reinterpret_cast<const uint4*>(new_v + tok_off);
     } else {
-      kv = *reinterpret_cast<const uint4*>(k_pages + cache_off);
+      kv = *reinterpret_cast<const uint4*>(kv_pages + k_off);
     }
     double x[8];
     unpack8(kv, x);
@@ -175,8 +177,8 @@ __global__ void __launch_bounds__(kThreads) summaries_append_kernel(
 
 }  // namespace
 
-cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16* k_pages,
-                                   kvsel_bf16* v_pages, int64_t n_pages, const int32_t* block_table,
+cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16* kv_pages,
+                                   int64_t n_pages, const int32_t* block_table,
                                    const int32_t* seq_lens, const int32_t* append_pos,
                                    const kvsel_bf16* new_k, const kvsel_bf16* new_v,
                                    kvsel_bf16* summaries, double* open_acc, int* err,
@@ -184,13 +186,13 @@ cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16*
   if (p.batch == 0) return cudaSuccess;
   if (mode == KVSEL_SUMMARY_FULL) {
     dim3 grid(p.max_blocks, p.batch);
-    summaries_full_kernel<<<grid, kThreads, 0, s>>>(k_pages, n_pages, block_table, seq_lens,
+    summaries_full_kernel<<<grid, kThreads, 0, s>>>(kv_pages, n_pages, block_table, seq_lens,
                                                     summaries, open_acc, p.n_kvheads, p.head_dim,
                                                     p.block_size, p.max_blocks, err);
   } else {
     summaries_append_kernel<<<p.batch, kThreads, 0, s>>>(
-        k_pages, v_pages, n_pages, block_table, append_pos, new_k, new_v, summaries, open_acc,
-        p.n_kvheads, p.head_dim, p.block_size, p.max_blocks, err);
+        kv_pages, n_pages, block_table, append_pos, new_k, new_v, summaries, open_acc, p.n_kvheads,
+        p.head_dim, p.block_size, p.max_blocks, err);
   }
   count_launch();
   return cudaGetLastError();

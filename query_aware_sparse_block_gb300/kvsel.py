@@ -50,7 +50,7 @@ class kvsel_problem(ctypes.Structure):
 
 class kvsel_kv_src(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("staging_slots", ctypes.c_int32),
-                ("k_pages", ctypes.c_void_p), ("v_pages", ctypes.c_void_p),
+                ("kv_pages", ctypes.c_void_p),
                 ("block_table", ctypes.c_void_p), ("n_pages", ctypes.c_int64),
                 ("staging", ctypes.c_void_p), ("host_kv", ctypes.c_void_p),
                 ("host_blocks", ctypes.c_int32), ("fetch_ctas", ctypes.c_int32)]
@@ -75,7 +75,7 @@ class kvsel_budget_out(ctypes.Structure):
 _P = ctypes.c_void_p
 _I = ctypes.c_int
 _SIGS = {
-    "kvsel_build_summaries": (_I, [ctypes.POINTER(kvsel_problem), _I, _P, _P, ctypes.c_int64, _P, _P,
+    "kvsel_build_summaries": (_I, [ctypes.POINTER(kvsel_problem), _I, _P, ctypes.c_int64, _P, _P,
                                    _P, _P, _P, _P, _P, _P]),
     "kvsel_score_topk": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, ctypes.c_float,
                               ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -189,16 +189,16 @@ def kvsel_get_error(stream=None) -> int:
     return int(lib().kvsel_get_error(_stream(stream)))
 
 
-def kvsel_build_summaries(p, mode, k_pages, v_pages, block_table, seq_lens, summaries, open_acc,
+def kvsel_build_summaries(p, mode, kv_pages, block_table, seq_lens, summaries, open_acc,
                           append_pos=None, new_k=None, new_v=None, stream=None):
-    for t, dt, n in ((k_pages, torch.bfloat16, "k_pages"), (v_pages, torch.bfloat16, "v_pages"),
+    for t, dt, n in ((kv_pages, torch.bfloat16, "kv_pages"),
                      (block_table, torch.int32, "block_table"), (seq_lens, torch.int32, "seq_lens"),
                      (summaries, torch.bfloat16, "summaries"), (open_acc, torch.float64, "open_acc"),
                      (append_pos, torch.int32, "append_pos"), (new_k, torch.bfloat16, "new_k"),
                      (new_v, torch.bfloat16, "new_v")):
         _expect(t, dt, n)
-    _check(lib().kvsel_build_summaries(ctypes.byref(p), mode, _ptr(k_pages), _ptr(v_pages),
-                                       k_pages.shape[0], _ptr(block_table), _ptr(seq_lens),
+    _check(lib().kvsel_build_summaries(ctypes.byref(p), mode, _ptr(kv_pages),
+                                       kv_pages.shape[0], _ptr(block_table), _ptr(seq_lens),
                                        _ptr(append_pos), _ptr(new_k), _ptr(new_v), _ptr(summaries),
                                        _ptr(open_acc), _stream(stream)),
            "kvsel_build_summaries")
@@ -250,14 +250,13 @@ def kvsel_merge_spans(p, sel_idx, n_sel, span_start, span_len, n_spans, stream=N
            "kvsel_merge_spans")
 
 
-def kv_paged(k_pages, v_pages, block_table) -> kvsel_kv_src:
-    _expect(k_pages, torch.bfloat16, "k_pages")
-    _expect(v_pages, torch.bfloat16, "v_pages")
+def kv_paged(kv_pages, block_table) -> kvsel_kv_src:
+    _expect(kv_pages, torch.bfloat16, "kv_pages")
     _expect(block_table, torch.int32, "block_table")
     s = kvsel_kv_src()
     s.kind = KVSEL_KV_PAGED
-    s.k_pages, s.v_pages, s.block_table = _ptr(k_pages), _ptr(v_pages), _ptr(block_table)
-    s.n_pages = k_pages.shape[0]
+    s.kv_pages, s.block_table = _ptr(kv_pages), _ptr(block_table)
+    s.n_pages = kv_pages.shape[0]
     return s
 
 

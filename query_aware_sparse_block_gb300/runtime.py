@@ -49,13 +49,13 @@ class SparseDecoder:
                             device=self.device),
                 torch.zeros((p.batch, p.n_kvheads, p.head_dim), dtype=torch.float64, device=self.device))
 
-    def build_summaries(self, k_pages, block_table, seq_lens, summaries, open_acc, stream=None):
-        K.kvsel_build_summaries(self.p, K.KVSEL_SUMMARY_FULL, k_pages, None, block_table, seq_lens,
+    def build_summaries(self, kv_pages, block_table, seq_lens, summaries, open_acc, stream=None):
+        K.kvsel_build_summaries(self.p, K.KVSEL_SUMMARY_FULL, kv_pages, block_table, seq_lens,
                                 summaries, open_acc, stream=stream)
 
-    def append(self, k_pages, v_pages, block_table, append_pos, summaries, open_acc, new_k=None,
+    def append(self, kv_pages, block_table, append_pos, summaries, open_acc, new_k=None,
                new_v=None, stream=None):
-        K.kvsel_build_summaries(self.p, K.KVSEL_SUMMARY_APPEND, k_pages, v_pages, block_table, None,
+        K.kvsel_build_summaries(self.p, K.KVSEL_SUMMARY_APPEND, kv_pages, block_table, None,
                                 summaries, open_acc, append_pos=append_pos, new_k=new_k, new_v=new_v,
                                 stream=stream)
 
@@ -86,17 +86,17 @@ class BoundLayer:
     to a few microseconds, so the host enqueues ahead of the GPU.
     """
 
-    def __init__(self, dec: SparseDecoder, q, k_pages, v_pages, block_table, summaries, open_acc,
+    def __init__(self, dec: SparseDecoder, q, kv_pages, block_table, summaries, open_acc,
                  out, lse, kv=None, gamma=2.0, tau_rel=0.0, new_k=None, new_v=None):
         L = K.lib()
         vp = ctypes.c_void_p
         self._fa, self._fs, self._fd = L.kvsel_build_summaries, L.kvsel_score_topk, L.kvsel_sparse_decode
         self.dec = dec
         self.p = ctypes.byref(dec.p)
-        self.kv = kv if kv is not None else K.kv_paged(k_pages, v_pages, block_table)
+        self.kv = kv if kv is not None else K.kv_paged(kv_pages, block_table)
         self.kv_ref = ctypes.byref(self.kv)
-        self.k_pages, self.v_pages = vp(k_pages.data_ptr()), vp(v_pages.data_ptr())
-        self.n_pages = int(k_pages.shape[0])
+        self.kv_pages = vp(kv_pages.data_ptr())
+        self.n_pages = int(kv_pages.shape[0])
         self.block_table = vp(block_table.data_ptr())
         self.q = vp(q.data_ptr())
         self.summ, self.acc = vp(summaries.data_ptr()), vp(open_acc.data_ptr())
@@ -115,7 +115,7 @@ class BoundLayer:
     def append(self, append_pos_ptr, stream_ptr, new_k_ptr=None, new_v_ptr=None):
         nk = new_k_ptr if new_k_ptr is not None else self.new_k
         nv = new_v_ptr if new_v_ptr is not None else self.new_v
-        rc = self._fa(self.p, K.KVSEL_SUMMARY_APPEND, self.k_pages, self.v_pages, self.n_pages,
+        rc = self._fa(self.p, K.KVSEL_SUMMARY_APPEND, self.kv_pages, self.n_pages,
                       self.block_table, None, append_pos_ptr, nk, nv, self.summ, self.acc, stream_ptr)
         if rc:
             K._check(rc, "kvsel_build_summaries")

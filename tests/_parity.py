@@ -47,8 +47,8 @@ def selection_verdict(scores: np.ndarray, k: int, gpu_sel: np.ndarray) -> str:
 def seq_inputs(x: dict, b: int, T: int):
     """bf16 bit arrays of sequence b: q [H_q][d], K and V [T][H_kv][d]."""
     qb = bits(x["q"][b])
-    kb = bits(logical_kv(x["k_pages"], x["block_table"], b, T))
-    vb = bits(logical_kv(x["v_pages"], x["block_table"], b, T))
+    kb = bits(logical_kv(x["kv_pages"], x["block_table"], b, T, 0))
+    vb = bits(logical_kv(x["kv_pages"], x["block_table"], b, T, 1))
     return qb, kb, vb
 
 

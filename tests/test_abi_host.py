@@ -113,7 +113,7 @@ def test_entry_points_validate_before_touching_the_device(K):
     rc = L.kvsel_sparse_decode(ctypes.byref(good), None, ctypes.byref(src), None, None, None, None,
                                None, None, None, 0.125, None, None, None, None, 0, None)
     assert rc == K.KVSEL_ERR_INVALID_ARG
-    rc = L.kvsel_build_summaries(ctypes.byref(good), 9, None, None, 0, None, None, None, None, None,
+    rc = L.kvsel_build_summaries(ctypes.byref(good), 9, None, 0, None, None, None, None, None,
                                  None, None, None)
     assert rc == K.KVSEL_ERR_INVALID_ARG
     assert b"mode" in L.kvsel_last_error()

@@ -49,14 +49,14 @@ def _decoder(w, x, k_max=None):
 def _run(K, w, x, k, gamma=2.0, tau_rel=0.0, k_per_seq=None, use_scores=True):
     dec = _decoder(w, x)
     summ, acc = dec.new_summaries()
-    dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
+    dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
     if k_per_seq is None:
         dec.k_per_seq.fill_(k)
     else:
         dec.k_per_seq.copy_(torch.as_tensor(k_per_seq, dtype=torch.int32))
     scores = torch.full((w.batch, x["max_blocks"]), float("nan"), device="cuda:0") if use_scores else None
     dec.select(x["q"], summ, x["seq_lens"], gamma=gamma, tau_rel=tau_rel, scores_out=scores)
-    dec.attend(x["q"], K.kv_paged(x["k_pages"], x["v_pages"], x["block_table"]), x["seq_lens"])
+    dec.attend(x["q"], K.kv_paged(x["kv_pages"], x["block_table"]), x["seq_lens"])
     torch.cuda.synchronize()
     return dec, summ, acc, scores
 
@@ -92,7 +92,7 @@ def test_incremental_append_equals_rebuild_and_writes_cache(K):
     x = to_dev(generate_layer(w, 0, max_blocks=8, seq_lens=[T0, T0 - 7]), "cuda:0")
     dec = _decoder(w, x)
     summ, acc = dec.new_summaries()
-    dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
+    dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
     g = torch.Generator(device="cuda:0")
     g.manual_seed(5)
     lens = x["seq_lens"].clone()
@@ -100,12 +100,12 @@ def test_incremental_append_equals_rebuild_and_writes_cache(K):
         new_k = torch.randn((w.batch, w.n_kvheads, w.head_dim), generator=g, device="cuda:0").to(torch.bfloat16)
         new_v = torch.randn((w.batch, w.n_kvheads, w.head_dim), generator=g, device="cuda:0").to(torch.bfloat16)
         pos = lens.clone()
-        dec.append(x["k_pages"], x["v_pages"], x["block_table"], pos, summ, acc, new_k=new_k, new_v=new_v)
+        dec.append(x["kv_pages"], x["block_table"], pos, summ, acc, new_k=new_k, new_v=new_v)
         lens += 1
     torch.cuda.synchronize()
     x["seq_lens"] = lens
     summ2, acc2 = dec.new_summaries()
-    dec.build_summaries(x["k_pages"], x["block_table"], lens, summ2, acc2)
+    dec.build_summaries(x["kv_pages"], x["block_table"], lens, summ2, acc2)
     torch.cuda.synchronize()
     for b in range(w.batch):
         T = int(lens[b])
@@ -124,7 +124,7 @@ def test_topk_exact_ties_take_lower_index(K):
     B = w.block_size
     tbl = x["block_table"][0]
     for n in range(40, 64):
-        x["k_pages"][tbl[n]] = x["k_pages"][tbl[n - 40]]
+        x["kv_pages"][tbl[n], :, 0] = x["kv_pages"][tbl[n - 40], :, 0]
     dec, summ, _, scores = _run(K, w, x, 20)
     sc = scores[0, :64].cpu().numpy()
     assert np.array_equal(sc[40:64], sc[0:24])
@@ -197,7 +197,7 @@ def test_bad_block_table_is_latched_not_fatal(K):
     x["block_table"][1, 3] = 10 ** 6
     dec = _decoder(w, x)
     summ, acc = dec.new_summaries()
-    dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
+    dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
     torch.cuda.synchronize()
     assert K.kvsel_get_error() == K.KVSEL_ERR_BOUNDS
     assert K.kvsel_get_error() == 0   # read-and-clear
@@ -208,7 +208,7 @@ def test_oversized_k_is_clamped_and_latched(K):
     x = to_dev(generate_layer(w, 0), "cuda:0")
     dec = _decoder(w, x, k_max=8)
     summ, acc = dec.new_summaries()
-    dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
+    dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
     dec.k_per_seq.fill_(12)
     dec.select(x["q"], summ, x["seq_lens"])
     torch.cuda.synchronize()
@@ -259,26 +259,26 @@ def test_c4_offload_tier_fetch_then_decode(K):
     k = w.k_for(w.keep_floor)
     x = generate_layer(w, 0, device="cuda:0", perm=False)
     N = w.n_blocks
-    tile = tuple(x["k_pages"].shape[1:])
-    host = torch.empty((w.batch, N, 2) + tile, dtype=torch.bfloat16, pin_memory=True)
-    host_tier_layout(x["k_pages"], x["v_pages"], x["block_table"], N, out=host)
+    page = tuple(x["kv_pages"].shape[1:])
+    host = torch.empty((w.batch, N) + page, dtype=torch.bfloat16, pin_memory=True)
+    host_tier_layout(x["kv_pages"], x["block_table"], N, out=host)
     dec = _decoder(w, x, k_max=N)
     summ, acc = dec.new_summaries()
-    dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
-    del x["v_pages"]
+    dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
+    del x["kv_pages"]
     torch.cuda.empty_cache()
     dec.k_per_seq.fill_(k)
     dec.select(x["q"], summ, x["seq_lens"], gamma=w.gamma)
     slots = k
-    staging = torch.empty((w.batch, slots, 2) + tile, dtype=torch.bfloat16, device="cuda:0")
+    staging = torch.empty((w.batch, slots) + page, dtype=torch.bfloat16, device="cuda:0")
     from query_aware_sparse_block_gb300 import kvsel as KK
     kv = KK.kv_host(host, N, staging, slots)
     dec.attend(x["q"], kv, x["seq_lens"])
     torch.cuda.synchronize()
     for b in (0, 31, 63):
         qb = bits(x["q"][b])
-        kb = bits(natural_blocks(host[b, :, 0]).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
-        vb = bits(natural_blocks(host[b, :, 1]).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
+        kb = bits(natural_blocks(host[b, :, :, 0]).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
+        vb = bits(natural_blocks(host[b, :, :, 1]).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
         sb, _, _ = o.block_summaries(kb, w.seq_len, w.block_size)
         sc = o.block_scores(qb, sb)
         gsel = dec.sel_idx[b, : int(dec.n_sel[b])].cpu().numpy()
@@ -287,7 +287,7 @@ def test_c4_offload_tier_fetch_then_decode(K):
         ref, _ = o.attend(qb, kb, vb, o.tokens_of_blocks(gsel, w.seq_len, w.block_size), dec.scale)
         emax, emean = attn_errors(dec.out[b].cpu().numpy(), ref)
         assert emax <= 1e-2 and emean <= 1e-3, (b, emax, emean)
-    # staging slot o holds the o-th selected block, K then V
+    # staging slot o holds the page of the o-th selected block
     b = 7
     gsel = dec.sel_idx[b, : int(dec.n_sel[b])].cpu()
     assert torch.equal(staging[b, :5].cpu(), host[b, gsel[:5].long()])

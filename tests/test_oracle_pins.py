@@ -396,7 +396,7 @@ def test_planted_needles_are_selected_at_both_keep_ratios(layer):
     x = generate_layer(w, layer)
     B = w.block_size
     for b in range(w.batch):
-        kb = bits(logical_kv(x["k_pages"], x["block_table"], b, w.seq_len))
+        kb = bits(logical_kv(x["kv_pages"], x["block_table"], b, w.seq_len, 0))
         s, _, _ = o.block_summaries(kb, w.seq_len, B)
         sc = o.block_scores(bits(x["q"][b]), s)
         for k in w.ks:
@@ -410,8 +410,8 @@ def test_planted_needles_are_selected_at_both_keep_ratios(layer):
 def test_c0_step_runs_and_is_self_consistent():
     w = C0
     x = generate_layer(w)
-    kb = bits(logical_kv(x["k_pages"], x["block_table"], 0, w.seq_len))
-    vb = bits(logical_kv(x["v_pages"], x["block_table"], 0, w.seq_len))
+    kb = bits(logical_kv(x["kv_pages"], x["block_table"], 0, w.seq_len, 0))
+    vb = bits(logical_kv(x["kv_pages"], x["block_table"], 0, w.seq_len, 1))
     r = o.decode_seq(bits(x["q"][0]), kb, vb, w.seq_len, w.block_size, w.topk, 1 / 8)
     assert len(r.sel) == w.topk and r.span_len.sum() == w.topk
     assert np.all(np.isfinite(r.out)) and np.all(np.isfinite(r.lse))

@@ -70,7 +70,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(K):
     dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size, x["max_blocks"],
                         k_max=40, device="cuda:0")
     summ, acc = dec.new_summaries()
-    dec.build_summaries(x["k_pages"], x["block_table"], x["seq_lens"], summ, acc)
+    dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
     dec.k_per_seq.copy_(torch.tensor([12, 5, 40, 7, 33], dtype=torch.int32))
     N = [(t + w.block_size - 1) // w.block_size for t in lens]
     scores = torch.zeros((w.batch, x["max_blocks"]), device="cuda:0")

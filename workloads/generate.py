@@ -12,14 +12,15 @@ draws q, then K, then V, each ~N(0, 1) in fp32 and rounded to bf16. Then:
   * drift: K[t, j, c] += amp * sin(2*pi*t/period + 2*pi*(j*d + c)/(H_kv*d)),
     added in fp32 before the bf16 rounding.
 
-Device layout (paged cache): K and V pages are [n_pages][H_kv][d/64][B][64]
-bf16 -- each (page, KV head) tile stores its B x d keys as d/64 column halves
-of B rows x 64 channels, and within every 128-byte row the 16-byte chunk c of
-token row t sits at chunk position c ^ (t % 8). ``to_tiled`` / ``from_tiled``
-convert between that and the natural [..., B, d] order. The block table
-[batch][max_blocks] int32 maps a sequence's logical block to its page.
-``perm=True`` scatters logical blocks over pages in a seeded random order so
-that every path goes through the table.
+Device layout (paged cache): one KV page array [n_pages][H_kv][2][d/64][B][64]
+bf16 -- for each (page, KV head) the K tile, then the V tile; each tile stores
+its B x d values as d/64 column halves of B rows x 64 channels, and within
+every 128-byte row the 16-byte chunk c of token row t sits at chunk position
+c ^ (t % 8). ``to_tiled`` / ``from_tiled`` convert between a tile and the
+natural [..., B, d] order. The block table [batch][max_blocks] int32 maps a
+sequence's logical block to its page. ``perm=True`` scatters logical blocks
+over pages in a seeded random order so that every path goes through the
+table.
 """
 from __future__ import annotations
 
@@ -73,7 +74,7 @@ def generate_layer(w: Workload, layer: int = 0, device="cpu", max_blocks: int | 
                    perm: bool = True, seq_lens=None, seed: int | None = None) -> dict:
     """Inputs of one layer of one decode step.
 
-    Returns dict with q [b][H_q][d] bf16, k_pages / v_pages [n_pages][H_kv][B][d]
+    Returns dict with q [b][H_q][d] bf16, kv_pages [n_pages][H_kv][2][d/64][B][64]
     bf16, block_table [b][max_blocks] int32 and seq_lens [b] int32 (all on
     ``device``). ``max_blocks`` may exceed the blocks in use (room to append).
     """
@@ -109,17 +110,16 @@ def generate_layer(w: Workload, layer: int = 0, device="cpu", max_blocks: int | 
     else:
         page_of = torch.arange(n_pages, dtype=torch.int32)
     block_table = page_of.view(b, MB).to(device)
-    k_pages = torch.empty((n_pages, Hkv, d // 64, B, 64), dtype=torch.bfloat16, device=device)
-    v_pages = torch.empty_like(k_pages)
+    kv_pages = torch.empty((n_pages, Hkv, 2, d // 64, B, 64), dtype=torch.bfloat16, device=device)
     idx = page_of.to(device=device, dtype=torch.long)
-    k_pages[idx] = to_tiled(kb.view(n_pages, Hkv, B, d))
+    kv_pages[idx, :, 0] = to_tiled(kb.view(n_pages, Hkv, B, d))
     del kb
-    v_pages[idx] = to_tiled(vb.view(n_pages, Hkv, B, d))
+    kv_pages[idx, :, 1] = to_tiled(vb.view(n_pages, Hkv, B, d))
     del vb
     if seq_lens is None:
         seq_lens = torch.full((b,), w.seq_len, dtype=torch.int32)
     seq_lens = torch.as_tensor(seq_lens, dtype=torch.int32).to(device)
-    return dict(q=q, k_pages=k_pages, v_pages=v_pages, block_table=block_table.contiguous(),
+    return dict(q=q, kv_pages=kv_pages, block_table=block_table.contiguous(),
                 seq_lens=seq_lens, max_blocks=MB)
 
 
@@ -128,12 +128,13 @@ def bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
-def logical_kv(pages: torch.Tensor, block_table: torch.Tensor, b: int, T: int) -> torch.Tensor:
-    """One sequence's cache in token order [T][H_kv][d], gathered from its pages."""
-    B = pages.shape[3]
+def logical_kv(kv_pages: torch.Tensor, block_table: torch.Tensor, b: int, T: int,
+               which: int) -> torch.Tensor:
+    """One sequence's keys (which=0) or values (which=1) in token order [T][H_kv][d]."""
+    B = kv_pages.shape[4]
     N = (T + B - 1) // B
-    p = block_table[b, :N].long().to(pages.device)
-    blk = from_tiled(pages[p])                      # [N][H_kv][B][d]
+    p = block_table[b, :N].long().to(kv_pages.device)
+    blk = from_tiled(kv_pages[p][:, :, which])      # [N][H_kv][B][d]
     return blk.permute(0, 2, 1, 3).reshape(N * B, blk.shape[1], blk.shape[3])[:T]
 
 
@@ -143,13 +144,13 @@ def natural_blocks(tiles: torch.Tensor) -> torch.Tensor:
     return x.transpose(-3, -2)
 
 
-def host_tier_layout(k_pages: torch.Tensor, v_pages: torch.Tensor, block_table: torch.Tensor,
-                     n_blocks: int, out: torch.Tensor | None = None) -> torch.Tensor:
-    """Offload-tier layout [b][N][2][page tile]: K then V of one block contiguous."""
+def host_tier_layout(kv_pages: torch.Tensor, block_table: torch.Tensor, n_blocks: int,
+                     out: torch.Tensor | None = None) -> torch.Tensor:
+    """Offload-tier layout [b][N][one page]: block n of sequence s is page block_table[s][n]."""
     b = block_table.shape[0]
     if out is None:
-        out = torch.empty((b, n_blocks, 2) + tuple(k_pages.shape[1:]), dtype=torch.bfloat16)
+        out = torch.empty((b, n_blocks) + tuple(kv_pages.shape[1:]), dtype=torch.bfloat16)
     for s in range(b):
-        p = block_table[s, :n_blocks].long().to(k_pages.device)
-        out[s].copy_(torch.stack([k_pages[p], v_pages[p]], dim=1))
+        p = block_table[s, :n_blocks].long().to(kv_pages.device)
+        out[s].copy_(kv_pages[p])
     return out
