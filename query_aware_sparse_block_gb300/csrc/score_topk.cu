@@ -433,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a) {
   int64_t prod_g = g0;
   int n_issued = 0;
   int q_issued_b = -1;
+  const uint64_t pol = l2_evict_first_policy();   // summaries are read once per step
   auto issue_next = [&]() {
     if (prod_g >= g1) return;
     int b, n0, nblk;
@@ -442,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a) {
     const uint32_t bytes = uint32_t(nblk) * block_bytes;
     const bool with_q = b != q_issued_b;
     mbar_arrive_expect_tx(bar, bytes + (with_q ? q_bytes : 0u));
-    bulk_load(dst, a.summaries + (int64_t(b) * a.max_blocks + n0) * NV * 8, bytes, bar);
+    bulk_load_hint(dst, a.summaries + (int64_t(b) * a.max_blocks + n0) * NV * 8, bytes, bar, pol);
     if (with_q) bulk_load(dst + kStageBytes, a.q + int64_t(b) * a.Hq * a.d, q_bytes, bar);
     q_issued_b = b;
     prod_g += nblk;

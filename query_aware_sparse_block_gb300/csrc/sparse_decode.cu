@@ -77,7 +77,7 @@ struct DecodeArgs {
   kvsel_bf16* out_bf16;
   float* lse;
   float* partials;     // warp states: [(cta + segment) * W + warp][G][D + 4] (m, l, -, -, O)
-  int* meta;           // [0] total tiles, [1] active CTAs, [2 ..] tile prefix per sequence
+  int2* seg_info;      // [batch * n_groups] (first CTA, CTA count) of each segment; count 0: no tile
   int* err;
   int batch, Hq, Hkv, G, B, max_blocks, k_max;
   int hpg, n_groups;   // heads per tile, head groups per sequence
@@ -223,10 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   const int64_t total = carry;
   const int A = int(min(int64_t(gridDim.x), max(int64_t(1), (total + kMinTilesPerCta - 1) / kMinTilesPerCta)));
   if (blockIdx.x == 0) {
-    for (int i = tid; i <= a.batch; i += kThreads) a.meta[2 + i] = base_s[i];
-    if (tid == 0) {
-      a.meta[0] = int(total);
-      a.meta[1] = A;
+    // the CTAs holding each segment's states, for the merge kernel
+    for (int64_t seg = tid; seg < int64_t(a.batch) * a.n_groups; seg += kThreads) {
+      const int b = int(seg / a.n_groups), hg = int(seg % a.n_groups);
+      const int seg_tiles = (base_s[b + 1] - base_s[b]) / a.n_groups;
+      int2 info = make_int2(0, 0);
+      if (seg_tiles > 0) {
+        const int64_t s_start = base_s[b] + int64_t(hg) * seg_tiles, s_end = s_start + seg_tiles;
+        const int first_c = int(((s_start + 1) * A - 1) / total);
+        const int last_c = int((s_end * A - 1) / total);
+        info = make_int2(first_c, last_c - first_c + 1);
+      }
+      a.seg_info[seg] = info;
     }
   }
 
@@ -280,11 +288,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
     rk = i < 32 ? rk0 : rk1;
     cnt = i < 32 ? c0 : c1;
   };
+  const uint64_t pol = l2_evict_first_policy();   // K/V are read once per step
   auto issue = [&](int m, int unit) {   // one lane
     uint64_t* bar = slot_bar(m);
     mbar_arrive_expect_tx(bar, uint32_t(tile_bytes));
     unsigned char* dst = tiles + size_t(slot_idx(m)) * tile_bytes;
-    bulk_load(dst, a.kv_base + int64_t(unit) * 2 * plane_elems, uint32_t(tile_bytes), bar);
+    bulk_load_hint(dst, a.kv_base + int64_t(unit) * 2 * plane_elems, uint32_t(tile_bytes), bar, pol);
   };
   if (active) {
     load_batch(0, cur_rk, cur_cnt);
@@ -539,33 +548,27 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
 // states costs one round trip to L2. Launched as a programmatic dependent of
 // the decode kernel: it can be resident early and waits for the decode grid's
 // completion before it reads anything that grid wrote.
-template <int D>
-__global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a, int wph) {
+template <int D, int WPH>
+__global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a) {
   constexpr int kCPL = D / 32;            // channels per lane
   constexpr int kChunk = 16;              // states in flight per lane
+  constexpr int kPerCta = kRings * WPH;   // warps of one CTA holding a head
   using vec_t = typename std::conditional<kCPL == 4, float4, float2>::type;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
   if (row >= int64_t(a.batch) * a.Hq) return;
   const int b = int(row / a.Hq), hq = int(row % a.Hq);
-  const int* base = a.meta + 2;
-  const int64_t total = __ldcg(a.meta);
-  const int A = __ldcg(a.meta + 1);
-  const int t0 = __ldcg(base + b), t1 = __ldcg(base + b + 1);
-  if (t1 == t0) return;                   // no attended token: written by the decode kernel
   const int G = a.G, j = hq / G, r = hq % G;
   const int hg = j / a.hpg, h_local = j % a.hpg;
-  const int seg_tiles = (t1 - t0) / a.n_groups;
-  const int64_t s_start = t0 + int64_t(hg) * seg_tiles, s_end = s_start + seg_tiles;
-  const int first_c = int(((s_start + 1) * A - 1) / total);
-  const int last_c = int((s_end * A - 1) / total);
   const int64_t seg = int64_t(b) * a.n_groups + hg;
-  const int per_cta = kRings * wph;       // warps of one CTA holding this head
-  const int NP = (last_c - first_c + 1) * per_cta;
+  const int2 info = __ldcg(a.seg_info + seg);
+  if (info.y == 0) return;                // no attended token: written by the decode kernel
+  const int first_c = info.x;
+  const int NP = info.y * kPerCta;
   auto state = [&](int i) -> const float* {
-    const int c = first_c + i / per_cta, k = i % per_cta;
-    const int w = (k / wph) * kRingWarps + h_local * wph + (k % wph);
+    const int c = first_c + i / kPerCta, k = i % kPerCta;
+    const int w = (k / WPH) * kRingWarps + h_local * WPH + (k % WPH);
     return a.partials + (((int64_t(c) + seg) * kW + w) * G + r) * (D + 4);
   };
   float M = -INFINITY, L = 0.f;           // running max and sum (log2 domain)
@@ -646,7 +649,7 @@ cudaError_t launch_t(const kvsel_problem& p, const DecodeArgs& a0, cudaStream_t 
   if (e != cudaSuccess) return e;
   // the row merge, as a programmatic dependent of the decode grid
   const unsigned merge_grid = unsigned((int64_t(p.batch) * p.n_qheads + 3) / 4);
-  e = launch_pdl(merge_rows_kernel<D>, dim3(merge_grid), dim3(128), 0, s, a, int(B / 16));
+  e = launch_pdl(merge_rows_kernel<D, B / 16>, dim3(merge_grid), dim3(128), 0, s, a);
   count_launch();
   return e;
 }
@@ -654,7 +657,8 @@ cudaError_t launch_t(const kvsel_problem& p, const DecodeArgs& a0, cudaStream_t 
 }  // namespace
 
 size_t decode_meta_bytes(const kvsel_problem& p) {
-  return (size_t(p.batch) * 4 + 3 * 4 + 255) / 256 * 256;
+  const int hpg = heads_per_group(p.block_size, p.n_kvheads);
+  return (size_t(p.batch) * (p.n_kvheads / hpg) * 8 + 255) / 256 * 256;
 }
 
 size_t sparse_decode_ws_bytes(const kvsel_problem& p) {
@@ -680,7 +684,7 @@ cudaError_t launch_sparse_decode(const kvsel_problem& p, const kvsel_bf16* q,
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = out; a.out_bf16 = out_bf16; a.lse = lse;
   char* w = static_cast<char*>(ws);
-  a.meta = reinterpret_cast<int*>(w);
+  a.seg_info = reinterpret_cast<int2*>(w);
   a.partials = reinterpret_cast<float*>(w + decode_meta_bytes(p));
   a.hpg = heads_per_group(p.block_size, p.n_kvheads);
   a.n_groups = p.n_kvheads / a.hpg;
