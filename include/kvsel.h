@@ -143,10 +143,10 @@ KVSEL_API int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16
  * kvsel_score_topk -- query-aware block score, Top-k and span merge
  * ("SparPR KV cache recovery on a consumer GPU", paragraphs "Query-Aware
  * key-block selection" and "On-demand local recomputation with cost-aware
- * fallback"). Enqueues two kernels on `stream` (scores, then Top-k), each
- * launched with programmatic stream serialization: a grid may become resident
- * while the kernel before it still runs, but reads no input before that
- * kernel has completed, so stream order is kept.
+ * fallback"). Enqueues two kernels on `stream` (scores, then Top-k). The
+ * score kernel is launched with programmatic stream serialization: it may
+ * become resident while the kernel before it still runs, but reads no input
+ * before that kernel has completed, so stream order is kept.
  *
  * score[b][n] = sum over query heads h of <q[b][h], summaries[b][n][kv(h)]>,
  * kv(h) = h / G, accumulated in fp32 (q is first folded over each GQA group).

@@ -4,8 +4,10 @@
 // recomputation with cost-aware fallback" for spans and the Dense Fallback
 // Threshold gamma).
 //
-// Design (GB300): two grids per call, chained by programmatic dependent
-// launch so that each is resident before its predecessor finishes.
+// Design (GB300): two grids per call. The score grid is launched with
+// programmatic stream serialization (resident while the kernel before it
+// finishes; it reads no input before griddepcontrol.wait); the Top-k grid is
+// an ordinary launch after it.
 //
 // score_kernel streams the summary table, the only large input. The flattened
 // list of (sequence, block) pairs is cut into equal contiguous ranges, one per
@@ -25,6 +27,8 @@
 // clustered rows fall back to a histogram search over the order keys), ties
 // at the k-th key are taken in index order, and block-wide scans emit the
 // ascending selection, the spans and the gamma decision.
+#include <type_traits>
+
 #include "kvsel_common.cuh"
 #include "kvsel_internal.h"
 
@@ -193,22 +197,25 @@ __device__ __forceinline__ int value_bin(float s, float smin, float scale) {
 // the (k - n_gt) lowest-index keys equal to K*.
 __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int N = seq_blocks(a, b);
   const int kreq = a.k_per_seq[b];
+  const float* sc = a.scores + int64_t(b) * a.max_blocks;
+  uint32_t* keys_s = sm.keys;
+  uint8_t* flags_s = sm.flags;
+  // the whole score row is read in the same round trip as the sequence length
+  // and k (entries past N are never used)
+#pragma unroll 4
+  for (int i = tid; i < a.max_blocks; i += kThreads) keys_s[i] = order_key(__ldcg(sc + i));
+  const int N = seq_blocks(a, b);
   if (kreq > a.k_max && tid == 0) latch_error(a.err, KVSEL_ERR_BOUNDS);
   int k = kreq < 0 ? 0 : kreq;
   k = min(k, min(N, a.k_max));
-  const float* sc = a.scores + int64_t(b) * a.max_blocks;
   const int KPT = (N + kThreads - 1) / kThreads;     // keys per thread, index order
   const int c0 = min(N, tid * KPT), c1 = min(N, c0 + KPT);
   const bool partial = k > 0 && k < N;
-  uint32_t* keys_s = sm.keys;
-  uint8_t* flags_s = sm.flags;
 
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int i = tid; i < N; i += kThreads) {
-    const uint32_t key = order_key(__ldcg(sc + i));
-    keys_s[i] = key;
+  for (int i = tid; i < N; i += kThreads) {   // entries this thread wrote above
+    const uint32_t key = keys_s[i];
     kmin = min(kmin, key);
     kmax = max(kmax, key);
   }
@@ -231,7 +238,7 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
     kstar = kmin;                            // one value: take the lowest indices
     n_eq = N;
   } else if (partial) {
-    bool done = false;
+    bool done = false, single = false;
     if (N <= kCand) {
       // few keys: rank them all
       for (int i = tid; i < N; i += kThreads) sm.cand[i] = keys_s[i];
@@ -248,7 +255,16 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
         __syncthreads();
         locate_bin(sm, k);
         const int bin = sm.bcast[0], above = sm.bcast[1], m = sm.bcast[2];
-        if (m <= kCand) {
+        if (m == 1) {
+          // a bin of one score: it is the k-th largest
+          for (int i = tid; i < N; i += kThreads)
+            if (value_bin(key_float(keys_s[i]), smin, scale) == bin) sm.bcast[4] = int(keys_s[i]);
+          __syncthreads();
+          kstar = uint32_t(sm.bcast[4]);
+          n_gt = above;
+          n_eq = 1;
+          single = true;
+        } else if (m <= kCand) {
           for (int i = tid; i < N; i += kThreads) {
             const uint32_t key = keys_s[i];
             if (value_bin(key_float(key), smin, scale) == bin) sm.cand[atomicAdd(&sm.bcast[7], 1)] = key;
@@ -260,7 +276,9 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
         }
       }
     }
-    if (done) {
+    if (single) {
+      // K* known: the one score of its bin
+    } else if (done) {
       kstar = uint32_t(sm.bcast[4]);
       n_gt += sm.bcast[5];
       n_eq = sm.bcast[6];
@@ -367,8 +385,6 @@ template <int VPL>
 __global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int scratch_s[kWarps];
-  // the Top-k grid may be scheduled now; it waits for this grid's completion
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int S = a.stages;
   const int SB = a.stage_bytes;
   unsigned char* stage = smem;                                               // [S][SB]
@@ -675,7 +691,10 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
   const size_t sel_smem = ((size_t(p.max_blocks) + 2) * 4 + size_t(p.max_blocks) + 127) / 128 * 128;
   e = ensure_smem(reinterpret_cast<const void*>(select_kernel), int(sel_smem));
   if (e != cudaSuccess) return e;
-  e = launch_pdl(select_kernel, dim3(p.batch), dim3(kThreads), sel_smem, s, a);
+  // An ordinary launch: made resident early, the Top-k CTAs would wait on SMs
+  // that still stream scores and slow that stream (measured: 0.9 us later end).
+  select_kernel<<<p.batch, kThreads, sel_smem, s>>>(a);
+  e = cudaGetLastError();
   count_launch();
   return e;
 }

@@ -32,30 +32,39 @@ def K():
     return kvsel
 
 
-def _rows(rng):
-    adj = (1.0 + rng.integers(0, 128, 5000) / 128.0).astype(np.float32)          # adjacent bf16 values
-    mixed = np.concatenate([rng.standard_normal(1500) * 1e-4, rng.standard_normal(1500) * 1e3])
-    straddle = np.full(3000, -1.0); straddle[:200] = 5.0; straddle[rng.choice(3000, 400, replace=False)] = 2.0
+def _rows(rng, nmax):
+    """Rows of at most nmax blocks; (scores, k) pairs."""
+    n = lambda x: min(x, nmax)
+    adj = (1.0 + rng.integers(0, 128, n(5000)) / 128.0).astype(np.float32)       # adjacent bf16 values
+    h = n(3000) // 2
+    mixed = np.concatenate([rng.standard_normal(h) * 1e-4, rng.standard_normal(h) * 1e3])
+    m = n(3000)
+    straddle = np.full(m, -1.0); straddle[: m // 15] = 5.0
+    straddle[rng.choice(m, m // 7, replace=False)] = 2.0
     return [
-        (rng.integers(-3, 4, 16384).astype(np.float64), 2048),       # 7 distinct values
-        (np.full(16384, 0.75), 100),                                # all equal
-        (adj.astype(np.float64), 777),
-        (rng.standard_normal(3000), 375),
-        (mixed, 300),
-        (straddle, 350),                                            # 200 above, take 150 of 400 tied
+        (rng.integers(-3, 4, nmax).astype(np.float64), nmax // 8),  # 7 distinct values
+        (np.full(nmax, 0.75), 100),                                 # all equal
+        (adj.astype(np.float64), n(5000) // 6),
+        (rng.standard_normal(n(3000)), n(3000) // 8),
+        (mixed, len(mixed) // 10),
+        (straddle, int((straddle > 2).sum()) + m // 20),            # ties at the k-th value straddle it
         (rng.integers(0, 3, 100).astype(np.float64), 37),           # short row: direct ranking
         (np.array([1.5]), 1),
         (rng.standard_normal(7), 0),
         (rng.standard_normal(129), 128),
-        (rng.standard_normal(16384), 16383),
+        (rng.standard_normal(nmax), nmax - 1),
+        (rng.standard_normal(nmax - 37), 1),
     ]
 
 
-def test_threshold_search_paths_match_oracle(K):
-    rng = np.random.default_rng(42)
-    rows = _rows(rng)
-    batch, Hkv, d, B, max_blocks = len(rows), 1, 64, 16, 16384
-    k_max = 16384
+@pytest.mark.parametrize("max_blocks", [1000, 2048, 16384])
+def test_threshold_search_paths_match_oracle(K, max_blocks):
+    """max_blocks 1000 and 2048 run the one-warp Top-k (32 and 64 keys per
+    lane); 16384 runs the CTA-wide one."""
+    rng = np.random.default_rng(42 + max_blocks)
+    rows = _rows(rng, max_blocks)
+    batch, Hkv, d, B = len(rows), 1, 64, 16
+    k_max = max_blocks
     dev = torch.device("cuda:0")
     p = K.problem(batch, 1, Hkv, d, B, max_blocks, k_max)
     summ = torch.zeros((batch, max_blocks, Hkv, d), dtype=torch.bfloat16)
