@@ -51,8 +51,27 @@ def parse():
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (debug)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-offload", action="store_true", help="skip the C4 offload-tier measurement")
     ap.add_argument("--ref-seqs", type=int, default=4, help="sequences per oracle sample")
     return ap.parse_args()
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over the ranks of the default process group
+    (the slowest replica's time is the job's time)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, layers: int, steps: int, elapsed_ms: float) -> float:
+    """Layer-steps per second of the whole job: every replica runs `steps`
+    steps of `layers` layers on its own sequences (weak scaling), and the job
+    takes as long as its slowest replica."""
+    return world * layers * steps / (elapsed_ms / 1e3)
 
 
 def dist_env():
@@ -383,9 +402,7 @@ def run_gpu(args):
         if err:
             raise RuntimeError(f"device error {err} in the timed region")
         if world > 1:
-            t = torch.tensor([elapsed_ms], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            elapsed_ms = float(t.item())
+            elapsed_ms = max_over_ranks(elapsed_ms, device)
         dec_ms = [a.elapsed_time(b) for a, b in zip(ev_s[1], ev_d[1])]
         sc_ms = [a.elapsed_time(b) for a, b in zip(ev_s[0], ev_s[1])]
 
@@ -422,7 +439,7 @@ def run_gpu(args):
                    "ms_per_step": e2e_ms, "steps": n_e2e}
 
     ms_per_step = elapsed_ms / args.steps
-    value = world * layers * args.steps / (elapsed_ms / 1e3)
+    value = whole_job_rate(world, layers, args.steps, elapsed_ms)
     peak, peak_kind = peaks()
     N = (wb.T0 + args.warmup + w.block_size) // w.block_size   # blocks at the first timed step
     dec_bytes = wb.decode_bytes()
@@ -461,12 +478,101 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": e2e,
     }
+    if world == 1 and not args.no_offload:
+        line["offload"] = run_offload(device, K)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_subprocess(args.ref_seqs, reps=5)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------ offload tier ---
+
+def run_offload(device, K, reps=5):
+    """C4 shape (64 sequences of 131072 tokens, 32 q / 2 KV heads, d 128, B 64):
+    the full K/V in pinned host memory, summaries on the GPU. Reports the
+    measured host-to-device copy rate of one large pinned copy, the budget
+    model's keep ratio and dense decision for this link, and for the keep
+    ratios 5 % (the floor) and 12.5 % the span gather (kvsel_fetch_spans) as
+    link bytes per second and as a fraction of the measured copy rate, plus
+    the whole offloaded decode (gather + attention)."""
+    import torch
+    from query_aware_sparse_block_gb300.runtime import SparseDecoder
+    from workloads import C4
+    from workloads.generate import generate_layer, host_tier_layout
+
+    w = C4
+    N = w.n_blocks
+    x = generate_layer(w, 0, device=device, perm=False)
+    page = tuple(x["kv_pages"].shape[1:])
+    page_bytes = int(np.prod(page)) * 2
+    host = torch.empty((w.batch, N) + page, dtype=torch.bfloat16, pin_memory=True)
+    host_tier_layout(x["kv_pages"], x["block_table"], N, out=host)
+    dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size, x["max_blocks"],
+                        k_max=N, device=device)
+    summ, acc = dec.new_summaries()
+    dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
+    torch.cuda.synchronize()
+    del x["kv_pages"]
+    torch.cuda.empty_cache()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(fn, n):
+        fn()
+        torch.cuda.synchronize()
+        ev[0].record()
+        for _ in range(n):
+            fn()
+        ev[1].record()
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[1]) / n / 1e3    # seconds per call
+
+    # the link's copy rate: one large pinned host -> device copy (2 GiB), best of 3
+    src = host.view(-1)[: 1 << 30]
+    dst = torch.empty(src.shape, dtype=src.dtype, device=device)
+    h2d_s = min(timed(lambda: dst.copy_(src, non_blocking=True), 1) for _ in range(3))
+    h2d_gbs = src.numel() * 2 / h2d_s / 1e9
+    del dst
+    torch.cuda.empty_cache()
+    peak_f = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak_f = json.load(f).get("bf16_tflops_sustained")
+    except (OSError, ValueError):
+        pass
+    flops = (peak_f or 1700.0) * 1e12
+    bud = K.kvsel_budget(w.block_size, w.n_kvheads, w.head_dim, 2, w.hidden, N, h2d_gbs * 1e9, flops,
+                         keep_floor=w.keep_floor, gamma=w.gamma)
+    res = {"workload": w.name, "h2d_copy_gbs": h2d_gbs, "h2d_copy_bytes": src.numel() * 2,
+           "budget_model": {"c_copy_s": bud.c_copy_s, "c_rec_s": bud.c_rec_s, "r_model": bud.r_model,
+                            "r": bud.r, "k": int(bud.k), "dense": bool(bud.dense),
+                            "recompute_flops_per_s": flops}}
+    for keep in (w.keep_floor, 0.125):
+        k = w.k_for(keep)
+        dec.k_per_seq.fill_(k)
+        dec.select(x["q"], summ, x["seq_lens"], gamma=w.gamma)
+        torch.cuda.synchronize()
+        n_dense = int(dec.dense_flag.sum())
+        staging = torch.empty((w.batch, k) + page, dtype=torch.bfloat16, device=device)
+        kv = K.kv_host(host, N, staging, k)
+        fetch_s = timed(lambda: K.kvsel_fetch_spans(dec.p, kv, x["seq_lens"], dec.span_start,
+                                                    dec.span_len, dec.n_spans, dec.dense_flag), reps)
+        link_bytes = int(dec.n_sel.sum()) * page_bytes
+        decode_s = timed(lambda: dec.attend(x["q"], kv, x["seq_lens"]), reps)
+        err = K.kvsel_get_error()
+        if err:
+            raise RuntimeError(f"device error {err} in the offload measurement")
+        res[f"keep_{keep:g}"] = {
+            "k": k, "dense_sequences": n_dense, "link_bytes_per_step": link_bytes,
+            "fetch_us": fetch_s * 1e6, "fetch_gbs": link_bytes / fetch_s / 1e9,
+            "frac_of_h2d_copy": link_bytes / fetch_s / 1e9 / h2d_gbs,
+            "fetch_plus_attend_us": decode_s * 1e6}
+        del staging
+    del host
+    torch.cuda.empty_cache()
+    return res
 
 
 # ------------------------------------------------------ oracle (reference) ---
