@@ -9,17 +9,21 @@
 // finishes; it reads no input before griddepcontrol.wait); the Top-k grid is
 // an ordinary launch after it.
 //
-// score_kernel streams the summary table, the only large input. The flattened
-// list of (sequence, block) pairs is cut into equal contiguous ranges, one per
-// CTA (one CTA per SM), with every cut moved to a chunk boundary of its
-// sequence. A CTA's range is cut into chunks of whole blocks of one sequence
-// (contiguous in memory); one thread moves each chunk into shared memory with
-// a 1-D bulk (TMA) copy, S chunks ahead, completions counted on mbarriers. The
-// query rows of a sequence ride along with the first chunk of that sequence
-// in the same stage, so folding q over its GQA group never waits on a global
-// load. Warps read block summaries from shared memory, multiply by the folded
-// query (fp32, in registers), reduce with shuffles and write one fp32 score
-// per block.
+// score_kernel streams the summary table, the only large input. The padded
+// list of (sequence, block) slots, max_blocks per sequence, is cut into equal
+// contiguous shares, one per CTA (one CTA per SM). No input decides the cut,
+// so the first copies leave right after the wait on the previous kernel. A
+// share is walked in chunks of up to 32 KiB of whole block summaries of one
+// sequence. A producer warp moves each chunk into shared memory with one 1-D
+// bulk (TMA) copy, S stages ahead: full / empty mbarrier pairs let it refill a
+// stage as soon as every consumer warp has released it, so the refill never
+// waits on a CTA-wide barrier. The first S chunks are copied before the
+// sequence lengths are read; later chunks stop at a sequence's last key block.
+// The query rows of a sequence ride with the first chunk of that sequence in
+// the same stage. Eight consumer warps fold q over its GQA group once per
+// sequence (shared memory, then registers), each warp reduces two block
+// summaries per pass against it (fp32 FMA, independent accumulators, shuffle
+// tree) and writes one fp32 score per block.
 //
 // select_kernel runs one CTA per sequence on those scores: a 2048-bin
 // histogram linear in the score value locates the bin holding the k-th
@@ -37,8 +41,10 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
+constexpr int kConsumerWarps = 8;        // score grid: warps that reduce summaries
+constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;   // plus one producer warp
 constexpr int kStageBytes = 32 * 1024;   // summary bytes per stage (query rows follow)
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 5;
 constexpr int kBins = 2048;               // histogram bins of the Top-k threshold search
 constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kCand = 128;                // bin size ranked exactly instead of refined
@@ -63,13 +69,16 @@ struct ScoreArgs {
   int chunk_blocks;    // blocks per bulk copy
   int stages;
   int stage_bytes;     // kStageBytes + query bytes of one sequence
-  int sel_offset;      // byte offset of the Top-k key / flag area in dynamic shared memory
 };
 
-__device__ __forceinline__ int seq_blocks(const ScoreArgs& a, int b) {
-  int T = a.seq_lens[b];
+// Key blocks of a sequence of T tokens in a row of max_blocks: ceil(T / B), T clamped.
+__device__ __forceinline__ int blocks_of_len(const ScoreArgs& a, int T) {
   T = T < 0 ? 0 : (T > a.max_blocks * a.B ? a.max_blocks * a.B : T);
   return (T + a.B - 1) / a.B;
+}
+
+__device__ __forceinline__ int seq_blocks(const ScoreArgs& a, int b) {
+  return blocks_of_len(a, a.seq_lens[b]);
 }
 
 // Order-preserving map of fp32 to uint32 (larger float -> larger key); -0 is
@@ -381,181 +390,232 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
   __syncthreads();
 }
 
+// Consumer warps only (the producer warp is not counted).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
 template <int VPL>
-__global__ void __launch_bounds__(kThreads, 1) score_kernel(ScoreArgs a) {
+__global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int scratch_s[kWarps];
   const int S = a.stages;
   const int SB = a.stage_bytes;
   unsigned char* stage = smem;                                               // [S][SB]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(S) * SB);
-  float* qf_s = reinterpret_cast<float*>(bars + kMaxStages);                 // Hkv*d floats
-  int* base_s = reinterpret_cast<int*>(qf_s + a.Hkv * a.d);                  // batch + 1
-
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * SB);       // copy landed
+  uint64_t* empty = full + kMaxStages;                                       // stage read
+  int* flag_s = reinterpret_cast<int*>(empty + kMaxStages);                  // [0] failure
+  float* qf_s = reinterpret_cast<float*>(flag_s + 4);                        // Hkv*d floats
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // Static share of the padded (sequence, block) slots. No input decides it,
+  // so it is known before the wait on the previous kernel and the first
+  // copies leave right after that wait. Chunks run from g0 in steps of CH
+  // blocks and stop at each row end.
+  const int64_t total = int64_t(a.batch) * a.max_blocks;
+  const int64_t g0 = total * blockIdx.x / gridDim.x;
+  const int64_t g1 = total * (blockIdx.x + 1) / gridDim.x;
+  if (g0 >= g1) return;
+  const int b_first = int(g0 / a.max_blocks);
+  const int n_first = int(g0 - int64_t(b_first) * a.max_blocks);
+  const int CH = a.chunk_blocks;
+  auto chunk_len = [&](int64_t g, int n0) {
+    return min(int(min(int64_t(CH), g1 - g)), a.max_blocks - n0);
+  };
+  // key blocks of sequence b from the token counts of the share's first 32
+  // sequences, one per lane (whole warp, b uniform)
+  int T_lane = 0;
+  auto n_of = [&](int b) {
+    const int i = b - b_first;
+    const int T = __shfl_sync(0xffffffffu, T_lane, i & 31);
+    return i < 32 ? blocks_of_len(a, T) : seq_blocks(a, b);
+  };
+  const int NV = a.NV;
+  const uint32_t block_bytes = uint32_t(NV) * 16;
+  const uint32_t q_bytes = uint32_t(a.Hq) * a.d * 2;
+
   if (tid == 0) {
-    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    flag_s[0] = 0;
     fence_barrier_init();
   }
+  __syncthreads();
   // every input may still be being written by an earlier kernel of the stream
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // exclusive prefix of blocks over sequences
-  int carry = 0;
-  for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
-    const int b = b0 + tid;
-    const int nb = b < a.batch ? seq_blocks(a, b) : 0;
-    int tot;
-    const int ex = block_exclusive_scan(nb, scratch_s, &tot);
-    if (b < a.batch) base_s[b] = carry + ex;
-    carry += tot;
-  }
-  if (tid == 0) base_s[a.batch] = carry;
-  __syncthreads();
-  const int64_t total = carry;
-  auto find_seq = [&](int64_t g) {
-    int lo = 0, hi = a.batch - 1;
-    while (lo < hi) {             // largest b with base_s[b] <= g
-      const int mid = (lo + hi + 1) >> 1;
-      if (base_s[mid] <= g) lo = mid; else hi = mid - 1;
+
+  if (warp == kConsumerWarps) {
+    // ---- producer warp: lane 0 refills a stage as soon as every consumer
+    // warp has released it. The first S chunks are copied whole before the
+    // sequence lengths are known (rows are max_blocks long, so the reads stay
+    // inside the table); later chunks stop at the last key block, and a chunk
+    // without one completes its stage with no copy. The query rows of a
+    // sequence ride with its first copied chunk. ----
+    const uint64_t pol = l2_evict_first_policy();   // summaries are read once per step
+    int q_b = -1;
+    int c = 0;
+    bool failed = false;
+    int b = b_first, n0 = n_first;
+    int nb_b = -1, nb = 0;            // key blocks of sequence nb_b
+    for (int64_t g = g0; g < g1; ++c) {
+      const int nblk = chunk_len(g, n0);
+      const int slot = c % S;
+      int nc = nblk;
+      if (c >= S) {
+        if (c == S) T_lane = b_first + lane < a.batch ? a.seq_lens[b_first + lane] : 0;
+        if (!mbar_wait_bounded(&empty[slot], uint32_t(((c / S) - 1) & 1))) {
+          if (lane == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
+          failed = true;
+        }
+        failed = __any_sync(0xffffffffu, failed) || *reinterpret_cast<volatile int*>(flag_s) != 0;
+        if (failed) break;
+        if (b != nb_b) {
+          nb = n_of(b);
+          nb_b = b;
+        }
+        nc = max(0, min(nblk, nb - n0));
+      }
+      if (lane == 0) {
+        if (nc > 0) {
+          const bool with_q = b != q_b;
+          const uint32_t bytes = uint32_t(nc) * block_bytes;
+          unsigned char* dst = stage + size_t(slot) * SB;
+          mbar_arrive_expect_tx(&full[slot], bytes + (with_q ? q_bytes : 0u));
+          bulk_load_hint(dst, a.summaries + (int64_t(b) * a.max_blocks + n0) * NV * 8, bytes,
+                         &full[slot], pol);
+          if (with_q) bulk_load(dst + kStageBytes, a.q + int64_t(b) * a.Hq * a.d, q_bytes, &full[slot]);
+        } else {
+          mbar_arrive(&full[slot]);
+        }
+      }
+      if (nc > 0) q_b = b;
+      g += nblk;
+      n0 += nblk;
+      if (n0 == a.max_blocks) { n0 = 0; ++b; }
     }
-    return lo;
-  };
-  const int CH = a.chunk_blocks;
-  // Equal shares of the flattened (sequence, block) list, each cut moved to
-  // the nearest chunk boundary of its sequence so that copies stay whole.
-  auto cut = [&](int64_t i) -> int64_t {
-    const int64_t g = total * i / gridDim.x;
-    const int b = find_seq(g);
-    const int N = base_s[b + 1] - base_s[b];
-    const int n = int(g - base_s[b]);
-    return base_s[b] + min(N, (n + CH / 2) / CH * CH);
-  };
-  const int64_t g0 = cut(blockIdx.x);
-  const int64_t g1 = blockIdx.x + 1 == gridDim.x ? total : cut(blockIdx.x + 1);
-  if (g0 >= g1) return;
+    // no copy may land after the CTA exits: after a failure, wait for the
+    // stages still in flight (the latest phase of each slot)
+    if (failed && lane == 0)
+      for (int i = max(0, c - S); i < c; ++i) (void)mbar_wait_bounded(&full[i % S], uint32_t((i / S) & 1));
+    return;
+  }
 
-  const int NV = a.NV;
-  const int block_bytes = NV * 16;
-  const uint32_t q_bytes = uint32_t(a.Hq) * a.d * 2;
-  // chunks of the range never cross a sequence end or the range end
-  auto chunk_at = [&](int64_t g, int& b, int& n0, int& nblk) {
-    b = find_seq(g);
-    n0 = int(g - base_s[b]);
-    const int64_t seq_end = base_s[b + 1];
-    nblk = int(min(int64_t(CH), min(seq_end, g1) - g));
-  };
-  // producer (thread 0): the next chunk to copy starts at prod_g; the query
-  // rows of a sequence travel with its first chunk in this CTA
-  int64_t prod_g = g0;
-  int n_issued = 0;
-  int q_issued_b = -1;
-  const uint64_t pol = l2_evict_first_policy();   // summaries are read once per step
-  auto issue_next = [&]() {
-    if (prod_g >= g1) return;
-    int b, n0, nblk;
-    chunk_at(prod_g, b, n0, nblk);
-    uint64_t* bar = &bars[n_issued % S];
-    unsigned char* dst = stage + size_t(n_issued % S) * SB;
-    const uint32_t bytes = uint32_t(nblk) * block_bytes;
-    const bool with_q = b != q_issued_b;
-    mbar_arrive_expect_tx(bar, bytes + (with_q ? q_bytes : 0u));
-    bulk_load_hint(dst, a.summaries + (int64_t(b) * a.max_blocks + n0) * NV * 8, bytes, bar, pol);
-    if (with_q) bulk_load(dst + kStageBytes, a.q + int64_t(b) * a.Hq * a.d, q_bytes, bar);
-    q_issued_b = b;
-    prod_g += nblk;
-    ++n_issued;
-  };
-  if (tid == 0)
-    for (int i = 0; i < S; ++i) issue_next();
-
+  // ---- consumer warps: block summaries against the query folded over its
+  // GQA group (fp32); a warp takes two blocks per pass with independent
+  // accumulators ----
   const int LPB = a.LPB, BPW = 32 / LPB;
   const int sub = lane / LPB, li = lane % LPB;
   const int G = a.Hq / a.Hkv;
+  const int HD = a.Hkv * a.d;
   float qreg[VPL <= 4 ? VPL : 1][8];
-  int cur_b = -1;
+  int cur_b = -1, N_cur = 0;
   bool dead = false;
+  int b = b_first, n0 = n_first;
+  T_lane = b_first + lane < a.batch ? a.seq_lens[b_first + lane] : 0;
   int c = 0;
   for (int64_t g = g0; g < g1; ++c) {
-    int b, n0, nblk;
-    chunk_at(g, b, n0, nblk);
-    if (!dead && !mbar_wait_bounded(&bars[c % S], uint32_t((c / S) & 1))) {
+    const int nblk = chunk_len(g, n0);
+    const int slot = c % S;
+    if (!dead && !mbar_wait_bounded(&full[slot], uint32_t((c / S) & 1))) {
       dead = true;
-      if (tid == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
+      *reinterpret_cast<volatile int*>(flag_s) = 1;
+      if (lane == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
     }
-    const unsigned char* st = stage + size_t(c % S) * SB;
+    const unsigned char* st = stage + size_t(slot) * SB;
     if (b != cur_b) {
-      // fold q over the GQA group, from the query rows that came with this chunk
+      // a new sequence, whose query rows came with this chunk: fold them over
+      // the GQA group once for the CTA, 8 channels per thread
       cur_b = b;
+      N_cur = n_of(b);
       const kvsel_bf16* qs = reinterpret_cast<const kvsel_bf16*>(st + kStageBytes);
+      consumer_sync();                // no warp still reads the previous fold
+      for (int v = tid; v < HD / 8; v += kConsumerWarps * 32) {
+        const int j = (v * 8) / a.d, cc = (v * 8) % a.d;
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        for (int r = 0; r < G; ++r) {
+          const uint4 x = *reinterpret_cast<const uint4*>(qs + (j * G + r) * a.d + cc);
+          f[0] += bf16lo(x.x); f[1] += bf16hi(x.x);
+          f[2] += bf16lo(x.y); f[3] += bf16hi(x.y);
+          f[4] += bf16lo(x.z); f[5] += bf16hi(x.z);
+          f[6] += bf16lo(x.w); f[7] += bf16hi(x.w);
+        }
+        float4* dq = reinterpret_cast<float4*>(qf_s + v * 8);
+        dq[0] = make_float4(f[0], f[1], f[2], f[3]);
+        dq[1] = make_float4(f[4], f[5], f[6], f[7]);
+      }
+      consumer_sync();
       if constexpr (VPL <= 4) {
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
-          const int e0 = (li + LPB * i) * 8;
-          const int j = e0 / a.d, cc = e0 % a.d;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) qreg[i][e] = 0.f;
-          for (int r = 0; r < G; ++r) {
-            const uint4 v = *reinterpret_cast<const uint4*>(qs + (j * G + r) * a.d + cc);
-            qreg[i][0] += bf16lo(v.x); qreg[i][1] += bf16hi(v.x);
-            qreg[i][2] += bf16lo(v.y); qreg[i][3] += bf16hi(v.y);
-            qreg[i][4] += bf16lo(v.z); qreg[i][5] += bf16hi(v.z);
-            qreg[i][6] += bf16lo(v.w); qreg[i][7] += bf16hi(v.w);
-          }
+          const float4* src = reinterpret_cast<const float4*>(qf_s + (li + LPB * i) * 8);
+          const float4 x0 = src[0], x1 = src[1];
+          qreg[i][0] = x0.x; qreg[i][1] = x0.y; qreg[i][2] = x0.z; qreg[i][3] = x0.w;
+          qreg[i][4] = x1.x; qreg[i][5] = x1.y; qreg[i][6] = x1.z; qreg[i][7] = x1.w;
         }
-      } else {
-        for (int e = tid; e < a.Hkv * a.d; e += kThreads) {
-          const int j = e / a.d, cc = e % a.d;
-          float acc = 0.f;
-          for (int r = 0; r < G; ++r) acc += __uint_as_float(uint32_t(qs[(j * G + r) * a.d + cc]) << 16);
-          qf_s[e] = acc;
-        }
-        __syncthreads();
       }
     }
-    if (!dead) {
+    const int nv = min(nblk, N_cur - n0);   // blocks of this chunk that hold keys
+    if (!dead && nv > 0) {
       float* out = a.scores + int64_t(b) * a.max_blocks + n0;
-      const int steps = (nblk + BPW - 1) / BPW;
-      for (int s = warp; s < steps; s += kWarps) {
-        const int r = s * BPW + sub;
-        float acc = 0.f;
-        if (r < nblk) {
+      const int steps = (nv + BPW - 1) / BPW;
+      for (int s0 = warp; s0 < steps; s0 += 2 * kConsumerWarps) {
+        const int r0 = s0 * BPW + sub;
+        const int r1 = r0 + kConsumerWarps * BPW;
+        // rows past nv read stage bytes that are never stored
+        const unsigned char* p0 = st + size_t(r0 < nv ? r0 : 0) * NV * 16;
+        const unsigned char* p1 = st + size_t(r1 < nv ? r1 : 0) * NV * 16;
+        float acc0 = 0.f, acc1 = 0.f;
+        constexpr int kUnroll = VPL <= 4 ? VPL : 4;
+#pragma unroll kUnroll
+        for (int i = 0; i < VPL; ++i) {
+          const uint4 v0 = *reinterpret_cast<const uint4*>(p0 + (li + LPB * i) * 16);
+          const uint4 v1 = *reinterpret_cast<const uint4*>(p1 + (li + LPB * i) * 16);
+          float qv[8];
+          if constexpr (VPL <= 4) {
 #pragma unroll
-          for (int i = 0; i < VPL; ++i) {
-            const uint4 v = *reinterpret_cast<const uint4*>(st + (size_t(r) * NV + li + LPB * i) * 16);
-            float qv[8];
-            if constexpr (VPL <= 4) {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) qv[e] = qreg[i][e];
-            } else {
-              const float4* src = reinterpret_cast<const float4*>(qf_s + (li + LPB * i) * 8);
-              const float4 x0 = src[0], x1 = src[1];
-              qv[0] = x0.x; qv[1] = x0.y; qv[2] = x0.z; qv[3] = x0.w;
-              qv[4] = x1.x; qv[5] = x1.y; qv[6] = x1.z; qv[7] = x1.w;
-            }
-            acc = fmaf(qv[0], bf16lo(v.x), acc);
-            acc = fmaf(qv[1], bf16hi(v.x), acc);
-            acc = fmaf(qv[2], bf16lo(v.y), acc);
-            acc = fmaf(qv[3], bf16hi(v.y), acc);
-            acc = fmaf(qv[4], bf16lo(v.z), acc);
-            acc = fmaf(qv[5], bf16hi(v.z), acc);
-            acc = fmaf(qv[6], bf16lo(v.w), acc);
-            acc = fmaf(qv[7], bf16hi(v.w), acc);
+            for (int e = 0; e < 8; ++e) qv[e] = qreg[i][e];
+          } else {
+            const float4* src = reinterpret_cast<const float4*>(qf_s + (li + LPB * i) * 8);
+            const float4 x0 = src[0], x1 = src[1];
+            qv[0] = x0.x; qv[1] = x0.y; qv[2] = x0.z; qv[3] = x0.w;
+            qv[4] = x1.x; qv[5] = x1.y; qv[6] = x1.z; qv[7] = x1.w;
           }
+          acc0 = fmaf(qv[0], bf16lo(v0.x), acc0);
+          acc1 = fmaf(qv[0], bf16lo(v1.x), acc1);
+          acc0 = fmaf(qv[1], bf16hi(v0.x), acc0);
+          acc1 = fmaf(qv[1], bf16hi(v1.x), acc1);
+          acc0 = fmaf(qv[2], bf16lo(v0.y), acc0);
+          acc1 = fmaf(qv[2], bf16lo(v1.y), acc1);
+          acc0 = fmaf(qv[3], bf16hi(v0.y), acc0);
+          acc1 = fmaf(qv[3], bf16hi(v1.y), acc1);
+          acc0 = fmaf(qv[4], bf16lo(v0.z), acc0);
+          acc1 = fmaf(qv[4], bf16lo(v1.z), acc1);
+          acc0 = fmaf(qv[5], bf16hi(v0.z), acc0);
+          acc1 = fmaf(qv[5], bf16hi(v1.z), acc1);
+          acc0 = fmaf(qv[6], bf16lo(v0.w), acc0);
+          acc1 = fmaf(qv[6], bf16lo(v1.w), acc1);
+          acc0 = fmaf(qv[7], bf16hi(v0.w), acc0);
+          acc1 = fmaf(qv[7], bf16hi(v1.w), acc1);
         }
-        for (int off = LPB >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (li == 0 && r < nblk) out[r] = acc;
+        for (int off = LPB >> 1; off > 0; off >>= 1) {
+          acc0 += __shfl_xor_sync(0xffffffffu, acc0, off);
+          acc1 += __shfl_xor_sync(0xffffffffu, acc1, off);
+        }
+        if (li == 0) {
+          if (r0 < nv) out[r0] = acc0;
+          if (r1 < nv) out[r1] = acc1;
+        }
       }
     }
-    __syncthreads();                  // every warp is done with this stage
-    if (tid == 0 && !dead) {
-      fence_proxy_async();
-      issue_next();
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);   // this warp is done with the stage
     g += nblk;
+    n0 += nblk;
+    if (n0 == a.max_blocks) { n0 = 0; ++b; }
   }
-  // no copy may land after the CTA exits: drain what a timeout left in flight
-  if (dead && tid == 0)
-    for (int i = c; i < n_issued; ++i) (void)mbar_wait_bounded(&bars[i % S], uint32_t((i / S) & 1));
 }
 
 // One CTA per sequence: Top-k, spans and the gamma decision on the scores the
@@ -651,11 +711,10 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
   a.chunk_blocks = std::max(1, kStageBytes / block_bytes);
   const size_t q_bytes = size_t(p.n_qheads) * p.head_dim * 2;
   a.stage_bytes = int((kStageBytes + q_bytes + 127) / 128 * 128);
-  // after the stages: barriers, folded q, sequence prefix
-  const size_t tail = size_t(kMaxStages) * 8 + size_t(p.n_kvheads) * p.head_dim * 4 +
-                      (size_t(p.batch) + 1) * 4;
+  // after the stages: full and empty barriers, a failure flag, folded q
+  const size_t tail = size_t(kMaxStages) * 16 + 16 + size_t(p.n_kvheads) * p.head_dim * 4;
   const int max_optin = max_smem_optin();
-  const size_t static_smem = kWarps * 4 + 256;
+  const size_t static_smem = 256;
   int stages = 0;
   for (int st = kMaxStages; st >= 1; --st)
     if (size_t(st) * a.stage_bytes + tail + static_smem <= size_t(max_optin)) {
@@ -673,7 +732,7 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
     auto kfn = score_kernel<V>;                                                              \
     e = ensure_smem(reinterpret_cast<const void*>(kfn), int(smem));                          \
     if (e != cudaSuccess) return e;                                                          \
-    e = launch_pdl(kfn, dim3(grid), dim3(kThreads), smem, s, a);                             \
+    e = launch_pdl(kfn, dim3(grid), dim3(kScoreThreads), smem, s, a);                        \
     break;                                                                                   \
   }
   switch (vpl) {
