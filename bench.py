@@ -250,11 +250,12 @@ class Workbench:
         rec = record or (lambda ev: ev.record(stream))
         self.budget_k()
         for l, bl in enumerate(self.bound):
-            bl.append(pos, sp, None if nk_ptrs is None else nk_ptrs[l],
-                      None if nv_ptrs is None else nv_ptrs[l])
             if ev_score is not None:
                 rec(ev_score[0][l])
-            bl.select(lens, sp, None if q_ptrs is None else q_ptrs[l])
+            # the token's summary update and the block selection, one call
+            bl.append_select(pos, lens, sp, None if nk_ptrs is None else nk_ptrs[l],
+                             None if nv_ptrs is None else nv_ptrs[l],
+                             None if q_ptrs is None else q_ptrs[l])
             if ev_score is not None:
                 rec(ev_score[1][l])
             bl.attend(lens, sp, None if q_ptrs is None else q_ptrs[l],
@@ -341,8 +342,9 @@ def run_gpu(args):
         # between two of them would turn that edge into a full dependency, so the
         # timing events sit on a side branch: each one waits for everything
         # enqueued on the main stream so far and records when that completes.
-        # A layer's score + Top-k time runs from the end of its append to the end
-        # of its Top-k grid; its decode time from there to the end of the merge.
+        # A layer's score + Top-k call (summary append folded in) runs from the
+        # end of the previous kernel to the end of its Top-k grid; its decode
+        # call from there to the end of the merge.
         cudart = load_cudart()
         side = torch.cuda.Stream(device=device)
         ssp = side.cuda_stream
@@ -472,9 +474,10 @@ def run_gpu(args):
         "host_capture_ms_per_step": host_ms,
         "timing": "one CUDA-graph replay of the timed steps (kernels launched through the C ABI "
                   "during capture, chained by programmatic dependent launch); per-call durations "
-                  "from external event nodes on a side branch of the graph: score_topk from the "
-                  "end of the layer's append to the end of its Top-k grid, sparse_decode from "
-                  "there to the end of its merge grid",
+                  "from external event nodes on a side branch of the graph: score_topk (the "
+                  "token's summary append folded in) from the end of the previous layer's merge "
+                  "grid to the end of its Top-k grid, sparse_decode from there to the end of its "
+                  "merge grid",
         "clocks": clk,
         "e2e": e2e,
     }

@@ -171,6 +171,47 @@ KVSEL_API int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, cons
                      int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
                      float* scores_out, void* ws, size_t ws_bytes, kvsel_stream_t stream);
 
+/* The inputs of the APPEND mode of kvsel_build_summaries, for the fused call
+ * below. Pointers are device pointers with the meaning, layout and alignment
+ * given there; new_k and new_v are nullable (new_v needs new_k). */
+typedef struct kvsel_append_in {
+  kvsel_bf16* kv_pages;           /* paged cache; the new K/V row is written into it */
+  int64_t n_pages;
+  const int32_t* block_table;     /* [batch][max_blocks] */
+  const int32_t* append_pos;      /* [batch]; t < 0 skips the sequence */
+  const kvsel_bf16* new_k;        /* [batch][n_kvheads][head_dim] or NULL */
+  const kvsel_bf16* new_v;        /* [batch][n_kvheads][head_dim] or NULL */
+  kvsel_bf16* summaries;          /* the summary table: updated, then scored */
+  double* open_acc;               /* [batch][n_kvheads][head_dim] fp64 */
+} kvsel_append_in;
+
+/*
+ * kvsel_append_score_topk -- kvsel_build_summaries(APPEND) followed by
+ * kvsel_score_topk on the updated table, in the two kernels of
+ * kvsel_score_topk (the decode step of "SparPR KV cache recovery on a
+ * consumer GPU", paragraph "Query-Aware key-block selection": the new token's
+ * key updates its block's summary before the query scores the blocks).
+ *
+ * Every output (kv_pages, summaries, open_acc, scores, selection, spans,
+ * dense_flag) equals, bit for bit, that of the two calls made in sequence on
+ * the same stream. seq_lens must already count the appended token
+ * (seq_lens[b] = append_pos[b] + 1 for an appending sequence). The append is
+ * done by the CTA whose share of the score work holds the open block, so it
+ * adds no kernel and no dependency step to the call.
+ *
+ * Arguments as kvsel_build_summaries (app) and kvsel_score_topk (the rest).
+ * Errors: INVALID_ARG (NULL app or required pointer, misalignment, new_v
+ * without new_k), UNSUPPORTED, WORKSPACE, CUDA; device BOUNDS as for the two
+ * calls.
+ */
+KVSEL_API int kvsel_append_score_topk(const kvsel_problem* p, const kvsel_append_in* app,
+                                      const kvsel_bf16* q, const int32_t* seq_lens,
+                                      const int32_t* k_per_seq, float gamma, float tau_rel,
+                                      int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                                      int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                                      float* scores_out, void* ws, size_t ws_bytes,
+                                      kvsel_stream_t stream);
+
 /*
  * kvsel_merge_spans -- span merge of an existing ascending selection ("SparPR
  * KV cache recovery on a consumer GPU", paragraph "On-demand local

@@ -245,6 +245,45 @@ int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16* kv_pages
                      "build_summaries launch");
 }
 
+static int score_topk_impl(const char* who, const kvsel_problem* p, const kvsel_bf16* q,
+                           const kvsel_bf16* summaries, const int32_t* seq_lens,
+                           const int32_t* k_per_seq, float gamma, float tau_rel, int32_t* sel_idx,
+                           int32_t* n_sel, int32_t* span_start, int32_t* span_len,
+                           int32_t* n_spans, uint8_t* dense_flag, float* scores_out, void* ws,
+                           size_t ws_bytes, const kvsel_append_in* app, kvsel_stream_t stream) {
+  char msg[160];
+  if (!q || !summaries || !seq_lens || !k_per_seq || !sel_idx || !n_sel || !span_start ||
+      !span_len || !n_spans) {
+    std::snprintf(msg, sizeof msg, "%s: NULL pointer", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (!aligned16(q) || !aligned16(summaries) || !aligned4(seq_lens) || !aligned4(k_per_seq) ||
+      !aligned4(sel_idx) || !aligned4(n_sel) || !aligned4(span_start) || !aligned4(span_len) ||
+      !aligned4(n_spans) || (scores_out && !aligned4(scores_out))) {
+    std::snprintf(msg, sizeof msg, "%s: misaligned pointer", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (!std::isfinite(gamma) || !std::isfinite(tau_rel) || tau_rel < 0) {
+    std::snprintf(msg, sizeof msg, "%s: gamma and tau_rel must be finite, tau_rel >= 0", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (!ws || ws_bytes < score_topk_ws_bytes(*p) || !aligned16(ws)) {
+    std::snprintf(msg, sizeof msg, "%s: workspace missing, small or misaligned", who);
+    return fail(KVSEL_ERR_WORKSPACE, msg);
+  }
+  int* ew = device_error_word();
+  if (!ew) {
+    std::snprintf(msg, sizeof msg, "%s: no CUDA device", who);
+    return fail(KVSEL_ERR_CUDA, msg);
+  }
+  std::snprintf(msg, sizeof msg, "%s launch", who);
+  return cuda_status(launch_score_topk(*p, q, summaries, seq_lens, k_per_seq, gamma, tau_rel,
+                                       sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
+                                       scores_out, ws, app, ew,
+                                       reinterpret_cast<cudaStream_t>(stream)),
+                     msg);
+}
+
 int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_bf16* summaries,
                      const int32_t* seq_lens, const int32_t* k_per_seq, float gamma,
                      float tau_rel, int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
@@ -253,23 +292,36 @@ int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_bf
   int r = check_problem(p);
   if (r) return r;
   if (p->batch == 0) return KVSEL_OK;
-  if (!q || !summaries || !seq_lens || !k_per_seq || !sel_idx || !n_sel || !span_start ||
-      !span_len || !n_spans)
-    return fail(KVSEL_ERR_INVALID_ARG, "score_topk: NULL pointer");
-  if (!aligned16(q) || !aligned16(summaries) || !aligned4(seq_lens) || !aligned4(k_per_seq) ||
-      !aligned4(sel_idx) || !aligned4(n_sel) || !aligned4(span_start) || !aligned4(span_len) ||
-      !aligned4(n_spans) || (scores_out && !aligned4(scores_out)))
-    return fail(KVSEL_ERR_INVALID_ARG, "score_topk: misaligned pointer");
-  if (!std::isfinite(gamma) || !std::isfinite(tau_rel) || tau_rel < 0)
-    return fail(KVSEL_ERR_INVALID_ARG, "score_topk: gamma and tau_rel must be finite, tau_rel >= 0");
-  if (!ws || ws_bytes < score_topk_ws_bytes(*p) || !aligned16(ws))
-    return fail(KVSEL_ERR_WORKSPACE, "score_topk: workspace missing, small or misaligned");
-  int* ew = device_error_word();
-  if (!ew) return fail(KVSEL_ERR_CUDA, "score_topk: no CUDA device");
-  return cuda_status(launch_score_topk(*p, q, summaries, seq_lens, k_per_seq, gamma, tau_rel,
-                                       sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
-                                       scores_out, ws, ew, reinterpret_cast<cudaStream_t>(stream)),
-                     "score_topk launch");
+  return score_topk_impl("score_topk", p, q, summaries, seq_lens, k_per_seq, gamma, tau_rel,
+                         sel_idx, n_sel, span_start, span_len, n_spans, dense_flag, scores_out,
+                         ws, ws_bytes, nullptr, stream);
+}
+
+int kvsel_append_score_topk(const kvsel_problem* p, const kvsel_append_in* app,
+                            const kvsel_bf16* q, const int32_t* seq_lens,
+                            const int32_t* k_per_seq, float gamma, float tau_rel,
+                            int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                            int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                            float* scores_out, void* ws, size_t ws_bytes,
+                            kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  if (!app) return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: NULL append inputs");
+  if (p->batch == 0) return KVSEL_OK;
+  if (!app->kv_pages || !app->block_table || !app->append_pos || !app->summaries ||
+      !app->open_acc || app->n_pages <= 0)
+    return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: NULL append pointer or no pages");
+  if (!aligned16(app->kv_pages) || !aligned16(app->summaries) || !aligned16(app->open_acc) ||
+      !aligned4(app->block_table) || !aligned4(app->append_pos) ||
+      (app->new_k && !aligned16(app->new_k)) || (app->new_v && !aligned16(app->new_v)))
+    return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: misaligned append pointer");
+  if (app->new_v && !app->new_k)
+    return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: new_v needs new_k");
+  if (app->n_pages * p->n_kvheads * 2 * p->block_size >= (int64_t(1) << 31))
+    return fail(KVSEL_ERR_UNSUPPORTED, "append_score_topk: more than 2^31 cache rows");
+  return score_topk_impl("append_score_topk", p, q, app->summaries, seq_lens, k_per_seq, gamma,
+                         tau_rel, sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
+                         scores_out, ws, ws_bytes, app, stream);
 }
 
 int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, const int32_t* n_sel,

@@ -29,14 +29,16 @@ cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16*
                                    kvsel_bf16* summaries, double* open_acc, int* err,
                                    cudaStream_t s);
 
-// ---- score + Top-k + spans (score_topk.cu) ----
+// ---- score + Top-k + spans (score_topk.cu); app != nullptr folds the
+// APPEND summary update into the score grid ----
 size_t score_topk_ws_bytes(const kvsel_problem& p);
 cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
                               const kvsel_bf16* summaries, const int32_t* seq_lens,
                               const int32_t* k_per_seq, float gamma, float tau_rel,
                               int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
                               int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
-                              float* scores_out, void* ws, int* err, cudaStream_t s);
+                              float* scores_out, void* ws, const kvsel_append_in* app,
+                              int* err, cudaStream_t s);
 cudaError_t launch_merge_spans(const kvsel_problem& p, const int32_t* sel_idx,
                                const int32_t* n_sel, int32_t* span_start, int32_t* span_len,
                                int32_t* n_spans, int* err, cudaStream_t s);

@@ -35,6 +35,7 @@
 
 #include "kvsel_common.cuh"
 #include "kvsel_internal.h"
+#include "summary_math.cuh"
 
 namespace kvsel {
 namespace {
@@ -42,7 +43,11 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kConsumerWarps = 8;        // score grid: warps that reduce summaries
-constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;   // plus one producer warp
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kAppendWarp0 = kConsumerWarps + 1;   // first of the append warps
+constexpr int kAppendWarps = 4;
+constexpr int kAppendThreads = kAppendWarps * 32;
+constexpr int kScoreThreads = (kConsumerWarps + 1 + kAppendWarps) * 32;
 constexpr int kStageBytes = 32 * 1024;   // summary bytes per stage (query rows follow)
 constexpr int kMaxStages = 5;
 constexpr int kBins = 2048;               // histogram bins of the Top-k threshold search
@@ -63,7 +68,16 @@ struct ScoreArgs {
   int32_t* n_spans;
   uint8_t* dense_flag;
   float* scores;       // [batch][max_blocks]
-    int* err;
+  int* err;
+  // the APPEND summary update folded into the call (append_pos == nullptr: none)
+  kvsel_bf16* kv_pages;
+  int64_t n_pages;
+  const int32_t* block_table;
+  const int32_t* append_pos;
+  const kvsel_bf16* new_k;
+  const kvsel_bf16* new_v;
+  kvsel_bf16* summaries_out;   // the table behind `summaries`
+  double* open_acc;
   int batch, Hq, Hkv, d, B, max_blocks, k_max;
   int NV, LPB;         // 16-byte vectors per block summary; lanes per block
   int chunk_blocks;    // blocks per bulk copy
@@ -395,6 +409,123 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// Append warps only.
+__device__ __forceinline__ void append_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kAppendThreads) : "memory");
+}
+
+// The APPEND summary update folded into the score grid, for the sequences
+// whose open block lies in this CTA's share of slots: the new K/V row goes
+// into its page, the block's fp64 key sum and summary are updated exactly as
+// the summary kernels do, and the block's score is computed from the new
+// summary. Run by the kAppendWarps append warps, one 8-channel vector per
+// thread, with every load issued before the page check so that the update
+// costs about two global round trips; it overlaps the first copies of the
+// share. The score then follows the consumers' arithmetic exactly: the lanes
+// li < LPB of the first append warp take the vectors li + LPB*i in order i
+// (the summary and the query folded in the consumers' order, from shared
+// scratch) and the shuffle tree is theirs, so the score equals, bit for bit,
+// the one a consumer computes from the updated summary; the consumers skip
+// that block. The bulk copy of the open block may carry either version of its
+// summary; the score computed from that copy is not stored.
+template <int VPL>
+__device__ void append_open_blocks(const ScoreArgs& a, int64_t g0, int64_t g1, uint4* sum_scr,
+                                   float* qf_scr) {
+  const int at = threadIdx.x - kAppendWarp0 * 32;   // 0 .. kAppendThreads-1
+  const int lane = at & 31;
+  const int NV = a.NV, LPB = a.LPB;
+  const int G = a.Hq / a.Hkv;
+  const int vec_per_head = a.d / 8;
+  const int b_first = int(g0 / a.max_blocks), b_last = int((g1 - 1) / a.max_blocks);
+  for (int b = b_first; b <= b_last; ++b) {
+    const int t = a.append_pos[b];
+    if (t < 0) continue;
+    if (t >= a.max_blocks * a.B) {
+      // reported once, by the CTA that holds the sequence's first slot
+      if (at == 0 && int64_t(b) * a.max_blocks >= g0) latch_error(a.err, KVSEL_ERR_BOUNDS);
+      continue;
+    }
+    const int n = t / a.B, row = t % a.B;
+    const int64_t gs = int64_t(b) * a.max_blocks + n;   // slot of the open block
+    if (gs < g0 || gs >= g1) continue;                   // another CTA's slot
+    const int64_t page = a.block_table[gs];
+    const bool scored = n < seq_blocks(a, b);           // the score call covers the block
+    const int64_t so = gs * a.Hkv * a.d;                 // the block's summary row
+    for (int v = at; v < NV; v += kAppendThreads) {
+      const int j = v / vec_per_head, c0 = (v % vec_per_head) * 8;
+      const int64_t tok_off = (int64_t(b) * a.Hkv + j) * a.d + c0;
+      // loads that do not need the page
+      uint4 kn = make_uint4(0, 0, 0, 0), vn = make_uint4(0, 0, 0, 0);
+      if (a.new_k) kn = *reinterpret_cast<const uint4*>(a.new_k + tok_off);
+      if (a.new_v) vn = *reinterpret_cast<const uint4*>(a.new_v + tok_off);
+      double* oa = a.open_acc + tok_off;
+      double prev[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) prev[e] = row == 0 ? 0.0 : oa[e];
+      float qf[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qf[e] = 0.f;
+      for (int r = 0; r < G; ++r) {
+        const uint4 x = *reinterpret_cast<const uint4*>(a.q + (int64_t(b) * a.Hq + j * G + r) * a.d + c0);
+        qf[0] += bf16lo(x.x); qf[1] += bf16hi(x.x);
+        qf[2] += bf16lo(x.y); qf[3] += bf16hi(x.y);
+        qf[4] += bf16lo(x.z); qf[5] += bf16hi(x.z);
+        qf[6] += bf16lo(x.w); qf[7] += bf16hi(x.w);
+      }
+      uint4 sv;
+      if (page >= 0 && page < a.n_pages) {
+        const int64_t k_off = (page * a.Hkv + j) * 2 * int64_t(a.B) * a.d + tiled_off(row, c0, a.B);
+        if (a.new_k) {
+          *reinterpret_cast<uint4*>(a.kv_pages + k_off) = kn;
+          if (a.new_v) *reinterpret_cast<uint4*>(a.kv_pages + k_off + int64_t(a.B) * a.d) = vn;
+        } else {
+          kn = *reinterpret_cast<const uint4*>(a.kv_pages + k_off);
+        }
+        double x[8], sum[8];
+        unpack8(kn, x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sum[e] = prev[e] + x[e];
+          oa[e] = sum[e];
+        }
+        sv = mean_to_bf16x8(sum, row + 1);
+        *reinterpret_cast<uint4*>(a.summaries_out + so + v * 8) = sv;
+      } else {
+        if (at == 0 && v == 0) latch_error(a.err, KVSEL_ERR_BOUNDS);
+        sv = *reinterpret_cast<const uint4*>(a.summaries + so + v * 8);   // left unchanged
+      }
+      sum_scr[v] = sv;
+      float4* q4 = reinterpret_cast<float4*>(qf_scr + v * 8);
+      q4[0] = make_float4(qf[0], qf[1], qf[2], qf[3]);
+      q4[1] = make_float4(qf[4], qf[5], qf[6], qf[7]);
+    }
+    append_sync();
+    if (at < 32) {
+      float acc = 0.f;
+      if (lane < LPB) {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int v = lane + LPB * i;
+          const uint4 sv = sum_scr[v];
+          const float4 x0 = reinterpret_cast<const float4*>(qf_scr + v * 8)[0];
+          const float4 x1 = reinterpret_cast<const float4*>(qf_scr + v * 8)[1];
+          acc = fmaf(x0.x, bf16lo(sv.x), acc);
+          acc = fmaf(x0.y, bf16hi(sv.x), acc);
+          acc = fmaf(x0.z, bf16lo(sv.y), acc);
+          acc = fmaf(x0.w, bf16hi(sv.y), acc);
+          acc = fmaf(x1.x, bf16lo(sv.z), acc);
+          acc = fmaf(x1.y, bf16hi(sv.z), acc);
+          acc = fmaf(x1.z, bf16lo(sv.w), acc);
+          acc = fmaf(x1.w, bf16hi(sv.w), acc);
+        }
+      }
+      for (int off = LPB >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (lane == 0 && scored) a.scores[gs] = acc;
+    }
+    append_sync();                    // the scratch is free for the next open block
+  }
+}
+
 template <int VPL>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -405,6 +536,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   uint64_t* empty = full + kMaxStages;                                       // stage read
   int* flag_s = reinterpret_cast<int*>(empty + kMaxStages);                  // [0] failure
   float* qf_s = reinterpret_cast<float*>(flag_s + 4);                        // Hkv*d floats
+  // append scratch (only with an append): NV summary vectors, NV*8 folded q
+  uint4* app_sum = reinterpret_cast<uint4*>(qf_s + a.Hkv * a.d);
+  float* app_qf = reinterpret_cast<float*>(app_sum + a.NV);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   // Static share of the padded (sequence, block) slots. No input decides it,
@@ -445,7 +579,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   // every input may still be being written by an earlier kernel of the stream
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  if (warp == kConsumerWarps) {
+  if (warp >= kAppendWarp0) {
+    if (a.append_pos) append_open_blocks<VPL>(a, g0, g1, app_sum, app_qf);
+    return;
+  }
+
+  if (warp == kProducerWarp) {
     // ---- producer warp: lane 0 refills a stage as soon as every consumer
     // warp has released it. The first S chunks are copied whole before the
     // sequence lengths are known (rows are max_blocks long, so the reads stay
@@ -510,9 +649,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   const int HD = a.Hkv * a.d;
   float qreg[VPL <= 4 ? VPL : 1][8];
   int cur_b = -1, N_cur = 0;
+  int n_open = -1;                    // block of cur_b whose score the append warp writes
   bool dead = false;
   int b = b_first, n0 = n_first;
   T_lane = b_first + lane < a.batch ? a.seq_lens[b_first + lane] : 0;
+  const int P_lane = a.append_pos && b_first + lane < a.batch ? a.append_pos[b_first + lane] : -1;
   int c = 0;
   for (int64_t g = g0; g < g1; ++c) {
     const int nblk = chunk_len(g, n0);
@@ -528,6 +669,12 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
       // the GQA group once for the CTA, 8 channels per thread
       cur_b = b;
       N_cur = n_of(b);
+      if (a.append_pos) {
+        const int i = b - b_first;
+        int t = __shfl_sync(0xffffffffu, P_lane, i & 31);
+        if (i >= 32) t = a.append_pos[b];
+        n_open = t >= 0 && t < a.max_blocks * a.B ? t / a.B : -1;
+      }
       const kvsel_bf16* qs = reinterpret_cast<const kvsel_bf16*>(st + kStageBytes);
       consumer_sync();                // no warp still reads the previous fold
       for (int v = tid; v < HD / 8; v += kConsumerWarps * 32) {
@@ -605,8 +752,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
           acc1 += __shfl_xor_sync(0xffffffffu, acc1, off);
         }
         if (li == 0) {
-          if (r0 < nv) out[r0] = acc0;
-          if (r1 < nv) out[r1] = acc1;
+          if (r0 < nv && n0 + r0 != n_open) out[r0] = acc0;
+          if (r1 < nv && n0 + r1 != n_open) out[r1] = acc1;
         }
       }
     }
@@ -689,10 +836,19 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
                               const int32_t* k_per_seq, float gamma, float tau_rel,
                               int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
                               int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
-                              float* scores_out, void* ws, int* err, cudaStream_t s) {
+                              float* scores_out, void* ws, const kvsel_append_in* app,
+                              int* err, cudaStream_t s) {
   if (p.batch == 0) return cudaSuccess;
   ScoreArgs a;
   a.q = q; a.summaries = summaries; a.seq_lens = seq_lens; a.k_per_seq = k_per_seq;
+  a.kv_pages = app ? app->kv_pages : nullptr;
+  a.n_pages = app ? app->n_pages : 0;
+  a.block_table = app ? app->block_table : nullptr;
+  a.append_pos = app ? app->append_pos : nullptr;
+  a.new_k = app ? app->new_k : nullptr;
+  a.new_v = app ? app->new_v : nullptr;
+  a.summaries_out = app ? app->summaries : nullptr;
+  a.open_acc = app ? app->open_acc : nullptr;
   a.gamma = gamma; a.tau_rel = tau_rel;
   a.sel_idx = sel_idx; a.n_sel = n_sel; a.span_start = span_start; a.span_len = span_len;
   a.n_spans = n_spans; a.dense_flag = dense_flag;
@@ -712,7 +868,8 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
   const size_t q_bytes = size_t(p.n_qheads) * p.head_dim * 2;
   a.stage_bytes = int((kStageBytes + q_bytes + 127) / 128 * 128);
   // after the stages: full and empty barriers, a failure flag, folded q
-  const size_t tail = size_t(kMaxStages) * 16 + 16 + size_t(p.n_kvheads) * p.head_dim * 4;
+  const size_t tail = size_t(kMaxStages) * 16 + 16 + size_t(p.n_kvheads) * p.head_dim * 4 +
+                      (app ? size_t(a.NV) * 48 : 0);
   const int max_optin = max_smem_optin();
   const size_t static_smem = 256;
   int stages = 0;

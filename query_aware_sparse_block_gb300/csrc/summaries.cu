@@ -3,56 +3,17 @@
 // key-block selection": a compact precomputed summary per block, resident on
 // the GPU), plus the incremental update as decode appends tokens.
 //
-// Arithmetic: each summary element is the fp64 sum of the block's keys taken
-// in token order from +0.0, divided by the token count in fp64 and rounded
-// once to bf16 (nearest, ties to even). The rounding from fp64 goes through
-// fp32 with round-to-odd, which gives the same result as one direct rounding
-// whenever the intermediate format carries at least two more bits than the
-// target (Boldo and Melquiond, "Emulation of FMA and correctly rounded sums:
-// proved algorithms using rounding to odd", IEEE Trans. Computers, 2008);
-// fp32 carries 24 bits against bf16's 8.
+// Arithmetic (summary_math.cuh): each summary element is the fp64 sum of the
+// block's keys in token order, divided by the token count and rounded once to
+// bf16.
 #include "kvsel_common.cuh"
 #include "kvsel_internal.h"
+#include "summary_math.cuh"
 
 namespace kvsel {
 namespace {
 
 constexpr int kThreads = 128;
-
-// Element offset, inside one K (or V) tile of a (page, head) in the tiled
-// layout, of the 8-channel vector starting at channel c0 (c0 % 8 == 0) of
-// token row t. The page of head j holds the K tile at element (page * H + j)
-// * 2 * B * d and the V tile right after it.
-__device__ __forceinline__ int64_t tiled_off(int t, int c0, int B) {
-  const int half = c0 >> 6, chunk = (c0 & 63) >> 3;
-  return (int64_t(half) * B + t) * 64 + ((chunk ^ (t & 7)) << 3);
-}
-
-__device__ __forceinline__ uint16_t f64_to_bf16_rne(double x) {
-  float f = __double2float_rz(x);
-  if (static_cast<double>(f) != x) f = __uint_as_float(__float_as_uint(f) | 1u);  // round to odd
-  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
-
-__device__ __forceinline__ void unpack8(const uint4& v, double (&x)[8]) {
-  x[0] = bf16lo(v.x); x[1] = bf16hi(v.x);
-  x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
-  x[4] = bf16lo(v.z); x[5] = bf16hi(v.z);
-  x[6] = bf16lo(v.w); x[7] = bf16hi(v.w);
-}
-
-__device__ __forceinline__ uint4 mean_to_bf16x8(const double (&acc)[8], int cnt) {
-  const double c = static_cast<double>(cnt);
-  uint16_t h[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) h[i] = f64_to_bf16_rne(acc[i] / c);
-  uint4 r;
-  r.x = h[0] | (uint32_t(h[1]) << 16);
-  r.y = h[2] | (uint32_t(h[3]) << 16);
-  r.z = h[4] | (uint32_t(h[5]) << 16);
-  r.w = h[6] | (uint32_t(h[7]) << 16);
-  return r;
-}
 
 // One CTA per (block n, sequence b). Threads own 8-channel column vectors of
 // one KV head and walk the block's tokens in order (pages in the tiled layout).

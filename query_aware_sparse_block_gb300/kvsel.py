@@ -48,6 +48,13 @@ class kvsel_problem(ctypes.Structure):
                 ("k_max", ctypes.c_int32)]
 
 
+class kvsel_append_in(ctypes.Structure):
+    _fields_ = [("kv_pages", ctypes.c_void_p), ("n_pages", ctypes.c_int64),
+                ("block_table", ctypes.c_void_p), ("append_pos", ctypes.c_void_p),
+                ("new_k", ctypes.c_void_p), ("new_v", ctypes.c_void_p),
+                ("summaries", ctypes.c_void_p), ("open_acc", ctypes.c_void_p)]
+
+
 class kvsel_kv_src(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("staging_slots", ctypes.c_int32),
                 ("kv_pages", ctypes.c_void_p),
@@ -79,6 +86,9 @@ _SIGS = {
                                    _P, _P, _P, _P, _P, _P]),
     "kvsel_score_topk": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, ctypes.c_float,
                               ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "kvsel_append_score_topk": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_append_in),
+                                     _P, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P, _P, _P, _P,
+                                     _P, _P, _P, ctypes.c_size_t, _P]),
     "kvsel_score_topk_noalloc": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, ctypes.c_float,
                                       ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvsel_noalloc_scratch_bytes": (ctypes.c_size_t, []),
@@ -220,6 +230,41 @@ def kvsel_score_topk(p, q, summaries, seq_lens, k_per_seq, sel_idx, n_sel, span_
                                   _ptr(dense_flag), _ptr(scores_out), _ptr(ws),
                                   ws.numel() * ws.element_size(), _stream(stream)),
            "kvsel_score_topk")
+
+
+def append_in(kv_pages, block_table, append_pos, summaries, open_acc, new_k=None,
+              new_v=None) -> kvsel_append_in:
+    """The APPEND inputs of kvsel_append_score_topk (kept alive by the caller
+    together with the tensors)."""
+    for t, dt, n in ((kv_pages, torch.bfloat16, "kv_pages"), (block_table, torch.int32, "block_table"),
+                     (append_pos, torch.int32, "append_pos"), (summaries, torch.bfloat16, "summaries"),
+                     (open_acc, torch.float64, "open_acc"), (new_k, torch.bfloat16, "new_k"),
+                     (new_v, torch.bfloat16, "new_v")):
+        _expect(t, dt, n)
+    a = kvsel_append_in()
+    a.kv_pages, a.n_pages = _ptr(kv_pages), kv_pages.shape[0]
+    a.block_table, a.append_pos = _ptr(block_table), _ptr(append_pos)
+    a.new_k, a.new_v = _ptr(new_k), _ptr(new_v)
+    a.summaries, a.open_acc = _ptr(summaries), _ptr(open_acc)
+    return a
+
+
+def kvsel_append_score_topk(p, app: kvsel_append_in, q, seq_lens, k_per_seq, sel_idx, n_sel,
+                            span_start, span_len, n_spans, ws, gamma=2.0, tau_rel=0.0,
+                            dense_flag=None, scores_out=None, stream=None):
+    """kvsel_build_summaries(APPEND) then kvsel_score_topk, in one call."""
+    for t, dt, n in ((q, torch.bfloat16, "q"), (seq_lens, torch.int32, "seq_lens"),
+                     (k_per_seq, torch.int32, "k_per_seq"), (sel_idx, torch.int32, "sel_idx"),
+                     (n_sel, torch.int32, "n_sel"), (span_start, torch.int32, "span_start"),
+                     (span_len, torch.int32, "span_len"), (n_spans, torch.int32, "n_spans"),
+                     (dense_flag, torch.uint8, "dense_flag"), (scores_out, torch.float32, "scores_out")):
+        _expect(t, dt, n)
+    _check(lib().kvsel_append_score_topk(ctypes.byref(p), ctypes.byref(app), _ptr(q), _ptr(seq_lens),
+                                         _ptr(k_per_seq), float(gamma), float(tau_rel), _ptr(sel_idx),
+                                         _ptr(n_sel), _ptr(span_start), _ptr(span_len), _ptr(n_spans),
+                                         _ptr(dense_flag), _ptr(scores_out), _ptr(ws),
+                                         ws.numel() * ws.element_size(), _stream(stream)),
+           "kvsel_append_score_topk")
 
 
 def kvsel_score_topk_noalloc(p, q, summaries, seq_lens, k_per_seq, sel_idx, n_sel, span_start,

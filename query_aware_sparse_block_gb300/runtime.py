@@ -67,6 +67,17 @@ class SparseDecoder:
                            gamma=gamma, tau_rel=tau_rel, dense_flag=self.dense_flag,
                            scores_out=scores_out, stream=stream)
 
+    def append_select(self, kv_pages, block_table, append_pos, q, summaries, open_acc, seq_lens,
+                      new_k=None, new_v=None, k_per_seq=None, gamma=2.0, tau_rel=0.0,
+                      scores_out=None, stream=None):
+        """append() then select() as one call (kvsel_append_score_topk)."""
+        kp = self.k_per_seq if k_per_seq is None else k_per_seq
+        app = K.append_in(kv_pages, block_table, append_pos, summaries, open_acc, new_k, new_v)
+        K.kvsel_append_score_topk(self.p, app, q, seq_lens, kp, self.sel_idx, self.n_sel,
+                                  self.span_start, self.span_len, self.n_spans, self.ws_score,
+                                  gamma=gamma, tau_rel=tau_rel, dense_flag=self.dense_flag,
+                                  scores_out=scores_out, stream=stream)
+
     def attend(self, q, kv, seq_lens, use_dense_flag=True, out=None, lse=None, out_bf16=None,
                stream=None):
         K.kvsel_sparse_decode(self.p, q, kv, seq_lens, self.sel_idx, self.n_sel,
@@ -91,6 +102,7 @@ class BoundLayer:
         L = K.lib()
         vp = ctypes.c_void_p
         self._fa, self._fs, self._fd = L.kvsel_build_summaries, L.kvsel_score_topk, L.kvsel_sparse_decode
+        self._fas = L.kvsel_append_score_topk
         self.dec = dec
         self.p = ctypes.byref(dec.p)
         self.kv = kv if kv is not None else K.kv_paged(kv_pages, block_table)
@@ -111,6 +123,11 @@ class BoundLayer:
         self.ws1, self.ws1n = vp(d.ws_score.data_ptr()), ctypes.c_size_t(d.ws_score.numel())
         self.ws2, self.ws2n = vp(d.ws_decode.data_ptr()), ctypes.c_size_t(d.ws_decode.numel())
         self.scale = ctypes.c_float(d.scale)
+        self._app = K.kvsel_append_in()
+        self._app.kv_pages, self._app.n_pages = self.kv_pages.value, self.n_pages
+        self._app.block_table = self.block_table.value
+        self._app.summaries, self._app.open_acc = self.summ.value, self.acc.value
+        self._app_ref = ctypes.byref(self._app)
 
     def append(self, append_pos_ptr, stream_ptr, new_k_ptr=None, new_v_ptr=None):
         nk = new_k_ptr if new_k_ptr is not None else self.new_k
@@ -119,6 +136,22 @@ class BoundLayer:
                       self.block_table, None, append_pos_ptr, nk, nv, self.summ, self.acc, stream_ptr)
         if rc:
             K._check(rc, "kvsel_build_summaries")
+
+    def append_select(self, append_pos_ptr, seq_lens_ptr, stream_ptr, new_k_ptr=None,
+                      new_v_ptr=None, q_ptr=None):
+        """append() and select() folded into one call (kvsel_append_score_topk)."""
+        app = self._app
+        app.append_pos = append_pos_ptr.value if isinstance(append_pos_ptr, ctypes.c_void_p) else append_pos_ptr
+        nk = new_k_ptr if new_k_ptr is not None else self.new_k
+        nv = new_v_ptr if new_v_ptr is not None else self.new_v
+        app.new_k = nk.value if isinstance(nk, ctypes.c_void_p) else nk
+        app.new_v = nv.value if isinstance(nv, ctypes.c_void_p) else nv
+        s = self.sel
+        rc = self._fas(self.p, self._app_ref, q_ptr if q_ptr is not None else self.q, seq_lens_ptr,
+                       self.kps, self.gamma, self.tau, s[0], s[1], s[2], s[3], s[4], s[5], None,
+                       self.ws1, self.ws1n, stream_ptr)
+        if rc:
+            K._check(rc, "kvsel_append_score_topk")
 
     def select(self, seq_lens_ptr, stream_ptr, q_ptr=None):
         s = self.sel

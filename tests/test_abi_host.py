@@ -32,7 +32,7 @@ def _declared_functions():
 
 def test_header_declares_the_entry_points():
     names = _declared_functions()
-    for n in ("kvsel_build_summaries", "kvsel_score_topk", "kvsel_merge_spans",
+    for n in ("kvsel_build_summaries", "kvsel_score_topk", "kvsel_append_score_topk", "kvsel_merge_spans",
               "kvsel_sparse_decode", "kvsel_budget", "kvsel_fetch_spans",
               "kvsel_workspace_size", "kvsel_kv_bytes_per_token", "kvsel_get_error",
               "kvsel_version"):
@@ -108,6 +108,22 @@ def test_entry_points_validate_before_touching_the_device(K):
     rc = L.kvsel_score_topk(ctypes.byref(good), None, None, None, None, 1.0, 0.0, None, None, None,
                             None, None, None, None, None, 0, None)
     assert rc == K.KVSEL_ERR_INVALID_ARG
+    # the fused append + score call: shape first, then the append inputs, then the rest
+    app = K.kvsel_append_in()
+    rc = L.kvsel_append_score_topk(ctypes.byref(bad), ctypes.byref(app), None, None, None, 1.0, 0.0,
+                                   None, None, None, None, None, None, None, None, 0, None)
+    assert rc == K.KVSEL_ERR_UNSUPPORTED
+    rc = L.kvsel_append_score_topk(ctypes.byref(good), None, None, None, None, 1.0, 0.0, None, None,
+                                   None, None, None, None, None, None, 0, None)
+    assert rc == K.KVSEL_ERR_INVALID_ARG
+    rc = L.kvsel_append_score_topk(ctypes.byref(good), ctypes.byref(app), None, None, None, 1.0, 0.0,
+                                   None, None, None, None, None, None, None, None, 0, None)
+    assert rc == K.KVSEL_ERR_INVALID_ARG and b"append" in L.kvsel_last_error()
+    app.kv_pages, app.n_pages, app.block_table, app.append_pos = 16, 4, 4, 4
+    app.summaries, app.open_acc, app.new_v = 16, 16, 16      # new_v without new_k
+    rc = L.kvsel_append_score_topk(ctypes.byref(good), ctypes.byref(app), None, None, None, 1.0, 0.0,
+                                   None, None, None, None, None, None, None, None, 0, None)
+    assert rc == K.KVSEL_ERR_INVALID_ARG and b"new_v" in L.kvsel_last_error()
     src = K.kvsel_kv_src()
     src.kind = 7
     rc = L.kvsel_sparse_decode(ctypes.byref(good), None, ctypes.byref(src), None, None, None, None,
