@@ -85,6 +85,28 @@ struct ScoreArgs {
   int stage_bytes;     // kStageBytes + query bytes of one sequence
 };
 
+// fp32 pairs for the packed FMA (fma.rn.f32x2: two IEEE fp32 FMAs, each
+// rounded as fmaf rounds). A block's score sums, per lane, its even channels
+// and its odd channels in two chains, adds them, and combines the lanes by the
+// xor tree; the consumers and the append warps both follow this order.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f32x2_sum(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// the two bf16 of a 32-bit word as an fp32 pair, the lower channel first
+__device__ __forceinline__ uint64_t bf16x2_f32x2(uint32_t w) { return f32x2(bf16lo(w), bf16hi(w)); }
+
 // Key blocks of a sequence of T tokens in a row of max_blocks: ceil(T / B), T clamped.
 __device__ __forceinline__ int blocks_of_len(const ScoreArgs& a, int T) {
   T = T < 0 ? 0 : (T > a.max_blocks * a.B ? a.max_blocks * a.B : T);
@@ -503,21 +525,23 @@ __device__ void append_open_blocks(const ScoreArgs& a, int64_t g0, int64_t g1, u
     if (at < 32) {
       float acc = 0.f;
       if (lane < LPB) {
+        float ev = 0.f, od = 0.f;      // even and odd channels, as the consumers' pairs
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int v = lane + LPB * i;
           const uint4 sv = sum_scr[v];
           const float4 x0 = reinterpret_cast<const float4*>(qf_scr + v * 8)[0];
           const float4 x1 = reinterpret_cast<const float4*>(qf_scr + v * 8)[1];
-          acc = fmaf(x0.x, bf16lo(sv.x), acc);
-          acc = fmaf(x0.y, bf16hi(sv.x), acc);
-          acc = fmaf(x0.z, bf16lo(sv.y), acc);
-          acc = fmaf(x0.w, bf16hi(sv.y), acc);
-          acc = fmaf(x1.x, bf16lo(sv.z), acc);
-          acc = fmaf(x1.y, bf16hi(sv.z), acc);
-          acc = fmaf(x1.z, bf16lo(sv.w), acc);
-          acc = fmaf(x1.w, bf16hi(sv.w), acc);
+          ev = fmaf(x0.x, bf16lo(sv.x), ev);
+          od = fmaf(x0.y, bf16hi(sv.x), od);
+          ev = fmaf(x0.z, bf16lo(sv.y), ev);
+          od = fmaf(x0.w, bf16hi(sv.y), od);
+          ev = fmaf(x1.x, bf16lo(sv.z), ev);
+          od = fmaf(x1.y, bf16hi(sv.z), od);
+          ev = fmaf(x1.z, bf16lo(sv.w), ev);
+          od = fmaf(x1.w, bf16hi(sv.w), od);
         }
+        acc = ev + od;
       }
       for (int off = LPB >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
       if (lane == 0 && scored) a.scores[gs] = acc;
@@ -647,7 +671,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   const int sub = lane / LPB, li = lane % LPB;
   const int G = a.Hq / a.Hkv;
   const int HD = a.Hkv * a.d;
-  float qreg[VPL <= 4 ? VPL : 1][8];
+  uint64_t qreg[VPL <= 4 ? VPL : 1][4];     // folded q, channel pairs
   int cur_b = -1, N_cur = 0;
   int n_open = -1;                    // block of cur_b whose score the append warp writes
   bool dead = false;
@@ -699,8 +723,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
         for (int i = 0; i < VPL; ++i) {
           const float4* src = reinterpret_cast<const float4*>(qf_s + (li + LPB * i) * 8);
           const float4 x0 = src[0], x1 = src[1];
-          qreg[i][0] = x0.x; qreg[i][1] = x0.y; qreg[i][2] = x0.z; qreg[i][3] = x0.w;
-          qreg[i][4] = x1.x; qreg[i][5] = x1.y; qreg[i][6] = x1.z; qreg[i][7] = x1.w;
+          qreg[i][0] = f32x2(x0.x, x0.y);
+          qreg[i][1] = f32x2(x0.z, x0.w);
+          qreg[i][2] = f32x2(x1.x, x1.y);
+          qreg[i][3] = f32x2(x1.z, x1.w);
         }
       }
     }
@@ -714,47 +740,44 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
         // rows past nv read stage bytes that are never stored
         const unsigned char* p0 = st + size_t(r0 < nv ? r0 : 0) * NV * 16;
         const unsigned char* p1 = st + size_t(r1 < nv ? r1 : 0) * NV * 16;
-        float acc0 = 0.f, acc1 = 0.f;
+        uint64_t acc0 = f32x2(0.f, 0.f), acc1 = f32x2(0.f, 0.f);   // (even, odd) channel sums
         constexpr int kUnroll = VPL <= 4 ? VPL : 4;
 #pragma unroll kUnroll
         for (int i = 0; i < VPL; ++i) {
           const uint4 v0 = *reinterpret_cast<const uint4*>(p0 + (li + LPB * i) * 16);
           const uint4 v1 = *reinterpret_cast<const uint4*>(p1 + (li + LPB * i) * 16);
-          float qv[8];
+          uint64_t qv[4];
           if constexpr (VPL <= 4) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) qv[e] = qreg[i][e];
+            for (int e = 0; e < 4; ++e) qv[e] = qreg[i][e];
           } else {
             const float4* src = reinterpret_cast<const float4*>(qf_s + (li + LPB * i) * 8);
             const float4 x0 = src[0], x1 = src[1];
-            qv[0] = x0.x; qv[1] = x0.y; qv[2] = x0.z; qv[3] = x0.w;
-            qv[4] = x1.x; qv[5] = x1.y; qv[6] = x1.z; qv[7] = x1.w;
+            qv[0] = f32x2(x0.x, x0.y);
+            qv[1] = f32x2(x0.z, x0.w);
+            qv[2] = f32x2(x1.x, x1.y);
+            qv[3] = f32x2(x1.z, x1.w);
           }
-          acc0 = fmaf(qv[0], bf16lo(v0.x), acc0);
-          acc1 = fmaf(qv[0], bf16lo(v1.x), acc1);
-          acc0 = fmaf(qv[1], bf16hi(v0.x), acc0);
-          acc1 = fmaf(qv[1], bf16hi(v1.x), acc1);
-          acc0 = fmaf(qv[2], bf16lo(v0.y), acc0);
-          acc1 = fmaf(qv[2], bf16lo(v1.y), acc1);
-          acc0 = fmaf(qv[3], bf16hi(v0.y), acc0);
-          acc1 = fmaf(qv[3], bf16hi(v1.y), acc1);
-          acc0 = fmaf(qv[4], bf16lo(v0.z), acc0);
-          acc1 = fmaf(qv[4], bf16lo(v1.z), acc1);
-          acc0 = fmaf(qv[5], bf16hi(v0.z), acc0);
-          acc1 = fmaf(qv[5], bf16hi(v1.z), acc1);
-          acc0 = fmaf(qv[6], bf16lo(v0.w), acc0);
-          acc1 = fmaf(qv[6], bf16lo(v1.w), acc1);
-          acc0 = fmaf(qv[7], bf16hi(v0.w), acc0);
-          acc1 = fmaf(qv[7], bf16hi(v1.w), acc1);
+          acc0 = ffma2(qv[0], bf16x2_f32x2(v0.x), acc0);
+          acc1 = ffma2(qv[0], bf16x2_f32x2(v1.x), acc1);
+          acc0 = ffma2(qv[1], bf16x2_f32x2(v0.y), acc0);
+          acc1 = ffma2(qv[1], bf16x2_f32x2(v1.y), acc1);
+          acc0 = ffma2(qv[2], bf16x2_f32x2(v0.z), acc0);
+          acc1 = ffma2(qv[2], bf16x2_f32x2(v1.z), acc1);
+          acc0 = ffma2(qv[3], bf16x2_f32x2(v0.w), acc0);
+          acc1 = ffma2(qv[3], bf16x2_f32x2(v1.w), acc1);
         }
-        for (int off = LPB >> 1; off > 0; off >>= 1) {
-          acc0 += __shfl_xor_sync(0xffffffffu, acc0, off);
-          acc1 += __shfl_xor_sync(0xffffffffu, acc1, off);
-        }
-        if (li == 0) {
-          if (r0 < nv && n0 + r0 != n_open) out[r0] = acc0;
-          if (r1 < nv && n0 + r1 != n_open) out[r1] = acc1;
-        }
+        // The xor tree of both blocks at once: at the first level the lanes
+        // with the LPB/2 bit keep block r1 and hand block r0 to their partner,
+        // the others the reverse; each later level works on one value. The
+        // sums are those of two separate trees.
+        const float sum0 = f32x2_sum(acc0), sum1 = f32x2_sum(acc1);
+        const int half = LPB >> 1;
+        const bool upper = (li & half) != 0;
+        float v = (upper ? sum1 : sum0) + __shfl_xor_sync(0xffffffffu, upper ? sum0 : sum1, half);
+        for (int off = half >> 1; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (li == 0 && r0 < nv && n0 + r0 != n_open) out[r0] = v;
+        if (li == half && r1 < nv && n0 + r1 != n_open) out[r1] = v;
       }
     }
     __syncwarp();
