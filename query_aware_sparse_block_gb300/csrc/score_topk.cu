@@ -161,6 +161,7 @@ struct SelectSmem {
   int* scratch;       // [kWarps] scan partials
   uint32_t* mm;       // [2 * kWarps] min / max partials
   int* bcast;         // [8]; bcast[7] is a gather counter, zero between uses
+  uint32_t* binkey;   // [kBins] a key that fell in each bin of the value histogram
 };
 
 // After a histogram of the candidates' bins: the bin holding the r-th largest
@@ -247,10 +248,19 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
   uint32_t* keys_s = sm.keys;
   uint8_t* flags_s = sm.flags;
   // the whole score row is read in the same round trip as the sequence length
-  // and k (entries past N are never used)
-#pragma unroll 4
-  for (int i = tid; i < a.max_blocks; i += kThreads) keys_s[i] = order_key(__ldcg(sc + i));
+  // and k (entries past N are never used); the row's min and max keys are
+  // taken on the way
   const int N = seq_blocks(a, b);
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll 4
+  for (int i = tid; i < a.max_blocks; i += kThreads) {
+    const uint32_t key = order_key(__ldcg(sc + i));
+    keys_s[i] = key;
+    if (i < N) {
+      kmin = min(kmin, key);
+      kmax = max(kmax, key);
+    }
+  }
   if (kreq > a.k_max && tid == 0) latch_error(a.err, KVSEL_ERR_BOUNDS);
   int k = kreq < 0 ? 0 : kreq;
   k = min(k, min(N, a.k_max));
@@ -258,12 +268,6 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
   const int c0 = min(N, tid * KPT), c1 = min(N, c0 + KPT);
   const bool partial = k > 0 && k < N;
 
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-  for (int i = tid; i < N; i += kThreads) {   // entries this thread wrote above
-    const uint32_t key = keys_s[i];
-    kmin = min(kmin, key);
-    kmax = max(kmax, key);
-  }
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
   if (lane == 0) {
@@ -295,17 +299,18 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
       const float span = __fsub_rn(smax, smin);
       const float scale = __fdiv_rn(float(kBins), span);
       if (isfinite(smin) && isfinite(span) && span > 0.f && isfinite(scale) && scale > 0.f) {
-        for (int i = tid; i < N; i += kThreads)
-          atomicAdd(&sm.hist[value_bin(key_float(keys_s[i]), smin, scale)], 1);
+        for (int i = tid; i < N; i += kThreads) {
+          const uint32_t key = keys_s[i];
+          const int bin = value_bin(key_float(key), smin, scale);
+          atomicAdd(&sm.hist[bin], 1);
+          sm.binkey[bin] = key;                // one of the bin's keys (the only one if m == 1)
+        }
         __syncthreads();
         locate_bin(sm, k);
         const int bin = sm.bcast[0], above = sm.bcast[1], m = sm.bcast[2];
         if (m == 1) {
           // a bin of one score: it is the k-th largest
-          for (int i = tid; i < N; i += kThreads)
-            if (value_bin(key_float(keys_s[i]), smin, scale) == bin) sm.bcast[4] = int(keys_s[i]);
-          __syncthreads();
-          kstar = uint32_t(sm.bcast[4]);
+          kstar = sm.binkey[bin];
           n_gt = above;
           n_eq = 1;
           single = true;
@@ -423,7 +428,6 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
       a.dense_flag[b] = (N > 0 && lhs >= rhs) ? 1 : 0;
     }
   }
-  __syncthreads();
 }
 
 // Consumer warps only (the producer warp is not counted).
@@ -793,6 +797,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(ScoreArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int hist_s[kBins];
+  __shared__ uint32_t binkey_s[kBins];
   __shared__ uint32_t cand_s[kCand];
   __shared__ int scratch_s[kWarps];
   __shared__ uint32_t mm_s[2 * kWarps];
@@ -810,6 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(ScoreArgs a) {
   sel.scratch = scratch_s;
   sel.mm = mm_s;
   sel.bcast = bcast_s;
+  sel.binkey = binkey_s;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   select_sequence(a, blockIdx.x, sel);
