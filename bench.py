@@ -250,8 +250,8 @@ class Workbench:
         rec = record or (lambda ev: ev.record(stream))
         self.budget_k()
         for l, bl in enumerate(self.bound):
-            if ev_score is not None:
-                rec(ev_score[0][l])
+            if ev_score is not None and l == 0:
+                rec(ev_score[0][0])             # later layers start at the previous merge's event
             # the token's summary update and the block selection, one call
             bl.append_select(pos, lens, sp, None if nk_ptrs is None else nk_ptrs[l],
                              None if nv_ptrs is None else nv_ptrs[l],
@@ -343,8 +343,9 @@ def run_gpu(args):
         # timing events sit on a side branch: each one waits for everything
         # enqueued on the main stream so far and records when that completes.
         # A layer's score + Top-k call (summary append folded in) runs from the
-        # end of the previous kernel to the end of its Top-k grid; its decode
-        # call from there to the end of the merge.
+        # end of the previous layer's merge grid (or the step's start) to the
+        # end of its Top-k grid; its decode call from there to the end of its
+        # merge grid.
         cudart = load_cudart()
         side = torch.cuda.Stream(device=device)
         ssp = side.cuda_stream
@@ -406,7 +407,12 @@ def run_gpu(args):
         if world > 1:
             elapsed_ms = max_over_ranks(elapsed_ms, device)
         dec_ms = [a.elapsed_time(b) for a, b in zip(ev_s[1], ev_d[1])]
-        sc_ms = [a.elapsed_time(b) for a, b in zip(ev_s[0], ev_s[1])]
+        # A layer's score call starts where the previous layer's decode call
+        # ended, on that same event: consecutive event nodes of the side branch
+        # fire about 2.5 us apart, so a second event at the same point would
+        # shift the start.
+        sc_start = [ev_s[0][i] if i % layers == 0 else ev_d[1][i - 1] for i in range(layers * args.steps)]
+        sc_ms = [a.elapsed_time(b) for a, b in zip(sc_start, ev_s[1])]
 
         # ---- e2e: pinned host inputs in, results out, through the public API ----
         e2e = None
