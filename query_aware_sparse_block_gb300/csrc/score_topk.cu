@@ -625,13 +625,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     bool failed = false;
     int b = b_first, n0 = n_first;
     int nb_b = -1, nb = 0;            // key blocks of sequence nb_b
+    int slot = 0, round = 0;          // c = round * S + slot
     for (int64_t g = g0; g < g1; ++c) {
       const int nblk = chunk_len(g, n0);
-      const int slot = c % S;
       int nc = nblk;
-      if (c >= S) {
+      if (round > 0) {
         if (c == S) T_lane = b_first + lane < a.batch ? a.seq_lens[b_first + lane] : 0;
-        if (!mbar_wait_bounded(&empty[slot], uint32_t(((c / S) - 1) & 1))) {
+        if (!mbar_wait_bounded(&empty[slot], uint32_t((round - 1) & 1))) {
           if (lane == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
           failed = true;
         }
@@ -660,6 +660,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
       g += nblk;
       n0 += nblk;
       if (n0 == a.max_blocks) { n0 = 0; ++b; }
+      if (++slot == S) { slot = 0; ++round; }
     }
     // no copy may land after the CTA exits: after a failure, wait for the
     // stages still in flight (the latest phase of each slot)
@@ -672,6 +673,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   // GQA group (fp32); a warp takes two blocks per pass with independent
   // accumulators ----
   const int LPB = a.LPB, BPW = 32 / LPB;
+  const int lg_bpw = __ffs(BPW) - 1;
   const int sub = lane / LPB, li = lane % LPB;
   const int G = a.Hq / a.Hkv;
   const int HD = a.Hkv * a.d;
@@ -682,11 +684,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
   int b = b_first, n0 = n_first;
   T_lane = b_first + lane < a.batch ? a.seq_lens[b_first + lane] : 0;
   const int P_lane = a.append_pos && b_first + lane < a.batch ? a.append_pos[b_first + lane] : -1;
-  int c = 0;
-  for (int64_t g = g0; g < g1; ++c) {
+  int slot = 0, round = 0;            // of the chunk in hand: round * S + slot
+  for (int64_t g = g0; g < g1;) {
     const int nblk = chunk_len(g, n0);
-    const int slot = c % S;
-    if (!dead && !mbar_wait_bounded(&full[slot], uint32_t((c / S) & 1))) {
+    if (!dead && !mbar_wait_bounded(&full[slot], uint32_t(round & 1))) {
       dead = true;
       *reinterpret_cast<volatile int*>(flag_s) = 1;
       if (lane == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
@@ -737,7 +738,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     const int nv = min(nblk, N_cur - n0);   // blocks of this chunk that hold keys
     if (!dead && nv > 0) {
       float* out = a.scores + int64_t(b) * a.max_blocks + n0;
-      const int steps = (nv + BPW - 1) / BPW;
+      const int steps = (nv + BPW - 1) >> lg_bpw;
       for (int s0 = warp; s0 < steps; s0 += 2 * kConsumerWarps) {
         const int r0 = s0 * BPW + sub;
         const int r1 = r0 + kConsumerWarps * BPW;
@@ -789,6 +790,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(ScoreArgs a) {
     g += nblk;
     n0 += nblk;
     if (n0 == a.max_blocks) { n0 = 0; ++b; }
+    if (++slot == S) { slot = 0; ++round; }
   }
 }
 
