@@ -38,11 +38,26 @@ __device__ __forceinline__ void unpack8(const uint4& v, double (&x)[8]) {
   x[6] = bf16lo(v.w); x[7] = bf16hi(v.w);
 }
 
+// x / c correctly rounded for a positive integer c, from r = RN(1/c): the
+// product q = RN(x r), its exact residual e = x - q c (one FMA) and the
+// corrected quotient RN(q + e r) (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Develop.
+// 34(1), 1990). fp64 division is slow on this part; one reciprocal then
+// serves the eight channels of a vector. A zero quotient keeps the sign of x.
+// Checked against IEEE division on 2^32 operands shaped like block sums.
+__device__ __forceinline__ double div_by_count(double x, double c, double r) {
+  const double q = x * r;
+  if (q == 0.0) return q;
+  const double e = fma(-q, c, x);
+  return fma(e, r, q);
+}
+
 __device__ __forceinline__ uint4 mean_to_bf16x8(const double (&acc)[8], int cnt) {
   const double c = static_cast<double>(cnt);
+  const double rc = 1.0 / c;
   uint16_t h[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) h[i] = f64_to_bf16_rne(acc[i] / c);
+  for (int i = 0; i < 8; ++i) h[i] = f64_to_bf16_rne(div_by_count(acc[i], c, rc));
   uint4 r;
   r.x = h[0] | (uint32_t(h[1]) << 16);
   r.y = h[2] | (uint32_t(h[3]) << 16);
