@@ -204,6 +204,23 @@ def topk_blocks(scores: np.ndarray, k: int) -> np.ndarray:
     return np.sort(order[:k]).astype(np.int64)
 
 
+def window_select(scores: np.ndarray, k: int, n_sink: int, n_recent: int) -> np.ndarray:
+    """Forced window plus Top-k over the remaining blocks, ascending.
+
+    [DKV] attends a dense recency window exactly beside the Top-k blocks. The
+    last ``n_recent`` blocks (and, by the same rule at the other end, the
+    first ``n_sink``) are taken whatever their score; the k largest scores
+    among the blocks in between are added (ties: lower index). With
+    n_sink = n_recent = 0 this is ``topk_blocks``.
+    """
+    N = len(scores)
+    lo = min(int(n_sink), N)
+    hi = max(lo, N - int(n_recent))
+    forced = list(range(0, lo)) + list(range(hi, N))
+    picked = [lo + int(i) for i in topk_blocks(np.asarray(scores, dtype=np.float64)[lo:hi], k)]
+    return np.array(sorted(forced + picked), dtype=np.int64)
+
+
 # ---------------------------------------------------------------------------
 # [SparPR] "On-demand local recomputation with cost-aware fallback": spans.
 # ---------------------------------------------------------------------------
@@ -336,17 +353,19 @@ class SeqStep:
 
 
 def decode_seq(q_bits, k_bits, v_bits, T: int, B: int, k: int, scale: float,
-               gamma: float = 2.0, tau_rel: float = 0.0, summary_bits=None) -> SeqStep:
+               gamma: float = 2.0, tau_rel: float = 0.0, summary_bits=None,
+               n_sink: int = 0, n_recent: int = 0) -> SeqStep:
     """Summaries -> scores -> Top-k -> spans -> gamma decision -> attention.
 
     ``gamma`` defaults to 2 (never dense for k <= N) so that callers opt in to
-    the fallback explicitly.
+    the fallback explicitly. ``n_sink`` / ``n_recent`` force the first / last
+    blocks into the selection (``window_select``).
     """
     N = n_blocks(T, B)
     if summary_bits is None:
         summary_bits, _, _ = block_summaries(k_bits, T, B) if T > 0 else (np.zeros((0,) + k_bits.shape[1:], np.uint16), None, None)
     scores = block_scores(q_bits, summary_bits) if N > 0 else np.zeros(0)
-    sel = topk_blocks(scores, k)
+    sel = window_select(scores, k, n_sink, n_recent)
     ss, sl = merge_spans(sel)
     dense = N > 0 and dense_fallback(len(ss), len(sel), N, gamma, tau_rel)
     blocks = np.arange(N) if dense else sel

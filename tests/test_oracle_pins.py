@@ -261,6 +261,48 @@ def test_topk_clamps_k():
     assert o.topk_blocks(np.zeros(0), 4).tolist() == []
 
 
+def _brute_window(scores, k, n_sink, n_recent):
+    """Every block set that holds the forced blocks and min(k, #candidates)
+    others, keeping the sets whose added blocks all score at least as high as
+    every candidate left out; among those the lowest indices win ties."""
+    N = len(scores)
+    forced = {i for i in range(N) if i < n_sink or i >= N - n_recent}
+    cands = [i for i in range(N) if i not in forced]
+    kk = max(0, min(k, len(cands)))
+    best = None
+    for sub in itertools.combinations(range(N), len(forced) + kk):
+        if not forced <= set(sub):
+            continue
+        added = [i for i in sub if i not in forced]
+        left = [i for i in cands if i not in sub]
+        if added and left and min(scores[i] for i in added) < max(scores[i] for i in left):
+            continue
+        key = sorted(added, key=lambda i: (-scores[i], i))
+        if best is None or [(-scores[i], i) for i in key] < [(-scores[i], i) for i in best[0]]:
+            best = (key, sorted(sub))
+    return best[1]
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_window_select_brute_force_with_ties(seed):
+    g = np.random.default_rng(100 + seed)
+    N = int(g.integers(0, 9))
+    scores = g.integers(-2, 3, size=N).astype(np.float64)
+    for n_sink in range(0, 3):
+        for n_recent in range(0, 4):
+            for k in range(0, N + 1):
+                got = o.window_select(scores, k, n_sink, n_recent).tolist()
+                assert got == _brute_window(list(scores), k, n_sink, n_recent), (scores, k, n_sink, n_recent)
+
+
+def test_zero_window_is_plain_topk():
+    g = np.random.default_rng(7)
+    for _ in range(50):
+        sc = g.standard_normal(int(g.integers(1, 40)))
+        k = int(g.integers(0, len(sc) + 1))
+        assert np.array_equal(o.window_select(sc, k, 0, 0), o.topk_blocks(sc, k))
+
+
 # ------------------------------------------------------------------ spans ---
 
 def test_spans_hand_examples(golden_dir):
@@ -333,6 +375,56 @@ def test_sparse_attention_equals_masked_library_attention():
     want = torch.nn.functional.scaled_dot_product_attention(
         q, K, V, attn_mask=torch.from_numpy(mask)[None, None, None, :], scale=scale)[0, :, 0].numpy()
     assert np.allclose(r.out, want, atol=1e-12, rtol=1e-10)
+
+
+def test_window_halves_merged_by_lse_equal_one_attention_over_the_union():
+    # [DKV]: the recency window is attended exactly, the Top-k blocks apart,
+    # and the two halves are merged by the log-sum-exp reduction. That merge
+    # must equal one softmax over the union of their tokens, which is what the
+    # oracle computes; both also match masked library attention.
+    g = np.random.default_rng(33)
+    Hq, Hkv, T, B, d = 8, 2, 300, 16, 32
+    qb = o.rne_bf16_bits(g.standard_normal((Hq, d)))
+    kb = o.rne_bf16_bits(g.standard_normal((T, Hkv, d)))
+    vb = o.rne_bf16_bits(g.standard_normal((T, Hkv, d)))
+    scale = 0.21
+    n_sink, n_recent, k = 1, 3, 4
+    r = o.decode_seq(qb, kb, vb, T, B, k, scale, n_sink=n_sink, n_recent=n_recent)
+    N = o.n_blocks(T, B)
+    window = [n for n in r.sel if n < n_sink or n >= N - n_recent]
+    topk = [n for n in r.sel if n_sink <= n < N - n_recent]
+    assert window == [0, N - 3, N - 2, N - 1] and len(topk) == k
+    o1, l1 = o.attend(qb, kb, vb, o.tokens_of_blocks(window, T, B), scale)
+    o2, l2 = o.attend(qb, kb, vb, o.tokens_of_blocks(topk, T, B), scale)
+    m = np.maximum(l1, l2)
+    w1, w2 = np.exp(l1 - m), np.exp(l2 - m)
+    merged = (w1[:, None] * o1 + w2[:, None] * o2) / (w1 + w2)[:, None]
+    assert np.allclose(r.out, merged, atol=1e-13, rtol=1e-11)
+    assert np.allclose(r.lse, m + np.log(w1 + w2), atol=1e-13, rtol=1e-13)
+    mask = np.zeros(T, dtype=bool)
+    for s in r.sel:
+        mask[s * B: min(T, s * B + B)] = True
+    q = torch.from_numpy(o.bf16_bits_to_f64(qb))[None, :, None, :]
+    K = torch.from_numpy(o.bf16_bits_to_f64(kb)).permute(1, 0, 2)[None].repeat_interleave(4, dim=1)
+    V = torch.from_numpy(o.bf16_bits_to_f64(vb)).permute(1, 0, 2)[None].repeat_interleave(4, dim=1)
+    want = torch.nn.functional.scaled_dot_product_attention(
+        q, K, V, attn_mask=torch.from_numpy(mask)[None, None, None, :], scale=scale)[0, :, 0].numpy()
+    assert np.allclose(r.out, want, atol=1e-12, rtol=1e-10)
+
+
+def test_window_covering_every_block_is_full_attention():
+    g = np.random.default_rng(34)
+    Hq, Hkv, T, B, d = 4, 2, 170, 32, 16
+    qb = o.rne_bf16_bits(g.standard_normal((Hq, d)))
+    kb = o.rne_bf16_bits(g.standard_normal((T, Hkv, d)))
+    vb = o.rne_bf16_bits(g.standard_normal((T, Hkv, d)))
+    want, want_lse = _sdpa_full(qb, kb, vb, T, 0.3)
+    N = o.n_blocks(T, B)
+    for n_sink, n_recent in ((0, N), (N, 0), (2, N - 2), (3, 9)):
+        r = o.decode_seq(qb, kb, vb, T, B, 1, 0.3, n_sink=n_sink, n_recent=n_recent)
+        assert r.sel.tolist() == list(range(N))
+        assert np.allclose(r.out, want, atol=1e-12, rtol=1e-10)
+        assert np.allclose(r.lse, want_lse, atol=1e-12, rtol=1e-12)
 
 
 def test_attention_closed_forms():
