@@ -212,6 +212,46 @@ KVSEL_API int kvsel_append_score_topk(const kvsel_problem* p, const kvsel_append
                                       float* scores_out, void* ws, size_t ws_bytes,
                                       kvsel_stream_t stream);
 
+/* Blocks attended whatever their score. */
+typedef struct kvsel_window {
+  int32_t n_sink;    /* the first n_sink blocks of every sequence */
+  int32_t n_recent;  /* the last n_recent blocks of every sequence (the recency window) */
+} kvsel_window;
+
+/*
+ * kvsel_score_topk_window -- kvsel_score_topk (or, with app != NULL,
+ * kvsel_append_score_topk) with a forced block window: the recency window
+ * that the DKV abstract ("DKV: Anchor + Low-Rank Differential KV-Cache
+ * Compression") attends exactly beside its Top-k blocks, merging the two
+ * parts by the flash-style log-sum-exp reduction. Here both parts go into one
+ * selection, so the split-K decode of kvsel_sparse_decode performs that
+ * merge. The leading n_sink blocks are the same rule at the start of the
+ * sequence (position-based keeping; the pages describe only the recency
+ * window).
+ *
+ * For sequence b with N_b blocks: the forced blocks are [0, lo) and [hi, N_b)
+ * with lo = min(n_sink, N_b), hi = max(lo, N_b - n_recent); the Top-k runs
+ * over the candidates [lo, hi) only, k_b = min(k_per_seq[b], hi - lo,
+ * k_max - F_b) of them (F_b = N_b - (hi - lo) forced blocks), ties to the
+ * lower index. sel_idx[b] holds the union in ascending order, n_sel[b] =
+ * F_b + k_b; spans and the gamma decision are taken on that union. A window
+ * of zero gives exactly the results of kvsel_score_topk.
+ *
+ * win: host pointer; n_sink >= 0, n_recent >= 0 and n_sink + n_recent <=
+ * k_max, else INVALID_ARG. k_per_seq[b] > k_max - F_b latches BOUNDS and is
+ * clamped. summaries: used when app == NULL; with app it must be NULL or
+ * app->summaries. Everything else as kvsel_score_topk and
+ * kvsel_append_score_topk, with the same errors.
+ */
+KVSEL_API int kvsel_score_topk_window(const kvsel_problem* p, const kvsel_window* win,
+                                      const kvsel_append_in* app, const kvsel_bf16* q,
+                                      const kvsel_bf16* summaries, const int32_t* seq_lens,
+                                      const int32_t* k_per_seq, float gamma, float tau_rel,
+                                      int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                                      int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                                      float* scores_out, void* ws, size_t ws_bytes,
+                                      kvsel_stream_t stream);
+
 /*
  * kvsel_merge_spans -- span merge of an existing ascending selection ("SparPR
  * KV cache recovery on a consumer GPU", paragraph "On-demand local

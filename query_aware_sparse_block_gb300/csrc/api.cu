@@ -250,7 +250,8 @@ static int score_topk_impl(const char* who, const kvsel_problem* p, const kvsel_
                            const int32_t* k_per_seq, float gamma, float tau_rel, int32_t* sel_idx,
                            int32_t* n_sel, int32_t* span_start, int32_t* span_len,
                            int32_t* n_spans, uint8_t* dense_flag, float* scores_out, void* ws,
-                           size_t ws_bytes, const kvsel_append_in* app, kvsel_stream_t stream) {
+                           size_t ws_bytes, const kvsel_append_in* app, int n_sink, int n_recent,
+                           kvsel_stream_t stream) {
   char msg[160];
   if (!q || !summaries || !seq_lens || !k_per_seq || !sel_idx || !n_sel || !span_start ||
       !span_len || !n_spans) {
@@ -279,7 +280,7 @@ static int score_topk_impl(const char* who, const kvsel_problem* p, const kvsel_
   std::snprintf(msg, sizeof msg, "%s launch", who);
   return cuda_status(launch_score_topk(*p, q, summaries, seq_lens, k_per_seq, gamma, tau_rel,
                                        sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
-                                       scores_out, ws, app, ew,
+                                       scores_out, ws, app, n_sink, n_recent, ew,
                                        reinterpret_cast<cudaStream_t>(stream)),
                      msg);
 }
@@ -294,7 +295,32 @@ int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_bf
   if (p->batch == 0) return KVSEL_OK;
   return score_topk_impl("score_topk", p, q, summaries, seq_lens, k_per_seq, gamma, tau_rel,
                          sel_idx, n_sel, span_start, span_len, n_spans, dense_flag, scores_out,
-                         ws, ws_bytes, nullptr, stream);
+                         ws, ws_bytes, nullptr, 0, 0, stream);
+}
+
+// Checks the inputs of a folded append; returns 0 or the failure code.
+static int check_append(const char* who, const kvsel_problem* p, const kvsel_append_in* app) {
+  char msg[160];
+  if (!app->kv_pages || !app->block_table || !app->append_pos || !app->summaries ||
+      !app->open_acc || app->n_pages <= 0) {
+    std::snprintf(msg, sizeof msg, "%s: NULL append pointer or no pages", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (!aligned16(app->kv_pages) || !aligned16(app->summaries) || !aligned16(app->open_acc) ||
+      !aligned4(app->block_table) || !aligned4(app->append_pos) ||
+      (app->new_k && !aligned16(app->new_k)) || (app->new_v && !aligned16(app->new_v))) {
+    std::snprintf(msg, sizeof msg, "%s: misaligned append pointer", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (app->new_v && !app->new_k) {
+    std::snprintf(msg, sizeof msg, "%s: new_v needs new_k", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (app->n_pages * p->n_kvheads * 2 * p->block_size >= (int64_t(1) << 31)) {
+    std::snprintf(msg, sizeof msg, "%s: more than 2^31 cache rows", who);
+    return fail(KVSEL_ERR_UNSUPPORTED, msg);
+  }
+  return KVSEL_OK;
 }
 
 int kvsel_append_score_topk(const kvsel_problem* p, const kvsel_append_in* app,
@@ -308,20 +334,40 @@ int kvsel_append_score_topk(const kvsel_problem* p, const kvsel_append_in* app,
   if (r) return r;
   if (!app) return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: NULL append inputs");
   if (p->batch == 0) return KVSEL_OK;
-  if (!app->kv_pages || !app->block_table || !app->append_pos || !app->summaries ||
-      !app->open_acc || app->n_pages <= 0)
-    return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: NULL append pointer or no pages");
-  if (!aligned16(app->kv_pages) || !aligned16(app->summaries) || !aligned16(app->open_acc) ||
-      !aligned4(app->block_table) || !aligned4(app->append_pos) ||
-      (app->new_k && !aligned16(app->new_k)) || (app->new_v && !aligned16(app->new_v)))
-    return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: misaligned append pointer");
-  if (app->new_v && !app->new_k)
-    return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: new_v needs new_k");
-  if (app->n_pages * p->n_kvheads * 2 * p->block_size >= (int64_t(1) << 31))
-    return fail(KVSEL_ERR_UNSUPPORTED, "append_score_topk: more than 2^31 cache rows");
+  r = check_append("append_score_topk", p, app);
+  if (r) return r;
   return score_topk_impl("append_score_topk", p, q, app->summaries, seq_lens, k_per_seq, gamma,
                          tau_rel, sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
-                         scores_out, ws, ws_bytes, app, stream);
+                         scores_out, ws, ws_bytes, app, 0, 0, stream);
+}
+
+int kvsel_score_topk_window(const kvsel_problem* p, const kvsel_window* win,
+                            const kvsel_append_in* app, const kvsel_bf16* q,
+                            const kvsel_bf16* summaries, const int32_t* seq_lens,
+                            const int32_t* k_per_seq, float gamma, float tau_rel,
+                            int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                            int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                            float* scores_out, void* ws, size_t ws_bytes,
+                            kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  if (!win) return fail(KVSEL_ERR_INVALID_ARG, "score_topk_window: NULL window");
+  if (win->n_sink < 0 || win->n_recent < 0 ||
+      int64_t(win->n_sink) + win->n_recent > int64_t(p->k_max))
+    return fail(KVSEL_ERR_INVALID_ARG,
+                "score_topk_window: need n_sink >= 0, n_recent >= 0, n_sink + n_recent <= k_max");
+  if (p->batch == 0) return KVSEL_OK;
+  if (app) {
+    r = check_append("score_topk_window", p, app);
+    if (r) return r;
+    if (summaries && summaries != app->summaries)
+      return fail(KVSEL_ERR_INVALID_ARG,
+                  "score_topk_window: with an append, summaries must be NULL or app->summaries");
+    summaries = app->summaries;
+  }
+  return score_topk_impl("score_topk_window", p, q, summaries, seq_lens, k_per_seq, gamma,
+                         tau_rel, sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
+                         scores_out, ws, ws_bytes, app, win->n_sink, win->n_recent, stream);
 }
 
 int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, const int32_t* n_sel,

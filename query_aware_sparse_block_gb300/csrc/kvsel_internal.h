@@ -30,7 +30,8 @@ cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16*
                                    cudaStream_t s);
 
 // ---- score + Top-k + spans (score_topk.cu); app != nullptr folds the
-// APPEND summary update into the score grid ----
+// APPEND summary update into the score grid; the first n_sink and the last
+// n_recent blocks of every sequence are selected whatever their score ----
 size_t score_topk_ws_bytes(const kvsel_problem& p);
 cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
                               const kvsel_bf16* summaries, const int32_t* seq_lens,
@@ -38,7 +39,7 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
                               int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
                               int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
                               float* scores_out, void* ws, const kvsel_append_in* app,
-                              int* err, cudaStream_t s);
+                              int n_sink, int n_recent, int* err, cudaStream_t s);
 cudaError_t launch_merge_spans(const kvsel_problem& p, const int32_t* sel_idx,
                                const int32_t* n_sel, int32_t* span_start, int32_t* span_len,
                                int32_t* n_spans, int* err, cudaStream_t s);

@@ -79,6 +79,7 @@ struct ScoreArgs {
   kvsel_bf16* summaries_out;   // the table behind `summaries`
   double* open_acc;
   int batch, Hq, Hkv, d, B, max_blocks, k_max;
+  int n_sink, n_recent;  // forced leading / trailing blocks of every sequence
   int NV, LPB;         // 16-byte vectors per block summary; lanes per block
   int chunk_blocks;    // blocks per bulk copy
   int stages;
@@ -231,6 +232,11 @@ __device__ __forceinline__ int value_bin(float s, float smin, float scale) {
 
 // Top-k + spans + gamma decision for sequence b (whole CTA).
 //
+// Forced blocks: the first n_sink and the last n_recent blocks of the
+// sequence are selected whatever their score (the recency window that the
+// DKV abstract attends exactly beside the Top-k blocks). The Top-k runs over
+// the candidate blocks [lo, hi) between them; with no window lo = 0, hi = N.
+//
 // Threshold: the k-th largest order key K* (with n_gt keys above it and n_eq
 // equal to it). Fast path: a histogram with 2048 bins linear in the score
 // value between the row's minimum and maximum finds the bin holding the k-th
@@ -251,22 +257,24 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
   // and k (entries past N are never used); the row's min and max keys are
   // taken on the way
   const int N = seq_blocks(a, b);
+  const int lo = min(a.n_sink, N), hi = max(lo, N - a.n_recent);   // candidates [lo, hi)
+  const int M = hi - lo, F = N - M;                                  // candidates, forced
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll 4
   for (int i = tid; i < a.max_blocks; i += kThreads) {
     const uint32_t key = order_key(__ldcg(sc + i));
     keys_s[i] = key;
-    if (i < N) {
+    if (i >= lo && i < hi) {
       kmin = min(kmin, key);
       kmax = max(kmax, key);
     }
   }
-  if (kreq > a.k_max && tid == 0) latch_error(a.err, KVSEL_ERR_BOUNDS);
+  if (kreq > a.k_max - F && tid == 0) latch_error(a.err, KVSEL_ERR_BOUNDS);
   int k = kreq < 0 ? 0 : kreq;
-  k = min(k, min(N, a.k_max));
+  k = min(k, min(M, a.k_max - F));
   const int KPT = (N + kThreads - 1) / kThreads;     // keys per thread, index order
   const int c0 = min(N, tid * KPT), c1 = min(N, c0 + KPT);
-  const bool partial = k > 0 && k < N;
+  const bool partial = k > 0 && k < M;
 
   kmin = __reduce_min_sync(0xffffffffu, kmin);
   kmax = __reduce_max_sync(0xffffffffu, kmax);
@@ -285,21 +293,21 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
   int n_gt = 0, n_eq = 0;
   if (partial && kmin == kmax) {
     kstar = kmin;                            // one value: take the lowest indices
-    n_eq = N;
+    n_eq = M;
   } else if (partial) {
     bool done = false, single = false;
-    if (N <= kCand) {
+    if (M <= kCand) {
       // few keys: rank them all
-      for (int i = tid; i < N; i += kThreads) sm.cand[i] = keys_s[i];
+      for (int i = tid; i < M; i += kThreads) sm.cand[i] = keys_s[lo + i];
       __syncthreads();
-      rank_candidates(sm, N, k);
+      rank_candidates(sm, M, k);
       done = true;
     } else {
       const float smin = key_float(kmin), smax = key_float(kmax);
       const float span = __fsub_rn(smax, smin);
       const float scale = __fdiv_rn(float(kBins), span);
       if (isfinite(smin) && isfinite(span) && span > 0.f && isfinite(scale) && scale > 0.f) {
-        for (int i = tid; i < N; i += kThreads) {
+        for (int i = lo + tid; i < hi; i += kThreads) {
           const uint32_t key = keys_s[i];
           const int bin = value_bin(key_float(key), smin, scale);
           atomicAdd(&sm.hist[bin], 1);
@@ -315,7 +323,7 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
           n_eq = 1;
           single = true;
         } else if (m <= kCand) {
-          for (int i = tid; i < N; i += kThreads) {
+          for (int i = lo + tid; i < hi; i += kThreads) {
             const uint32_t key = keys_s[i];
             if (value_bin(key_float(key), smin, scale) == bin) sm.cand[atomicAdd(&sm.bcast[7], 1)] = key;
           }
@@ -333,16 +341,16 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
       n_gt += sm.bcast[5];
       n_eq = sm.bcast[6];
     } else {
-      uint32_t lo = kmin;     // window: lo <= key, (key - lo) < 2^wbits (wbits 32: no upper bound)
+      uint32_t klo = kmin;    // key window: klo <= key, (key - klo) < 2^wbits (wbits 32: no upper bound)
       int wbits = 32;
       int r = k;              // rank of K* from the top among the window's keys
-      int m = N;              // keys in the window
+      int m = M;              // keys in the window
       int shift = max(0, (32 - __clz(int(kmax - kmin))) - 11);
       while (true) {
-        for (int i = tid; i < N; i += kThreads) {
+        for (int i = lo + tid; i < hi; i += kThreads) {
           const uint32_t key = keys_s[i];
-          const uint32_t dl = key - lo;
-          if (key >= lo && (wbits == 32 || (dl >> wbits) == 0u)) atomicAdd(&sm.hist[dl >> shift], 1);
+          const uint32_t dl = key - klo;
+          if (key >= klo && (wbits == 32 || (dl >> wbits) == 0u)) atomicAdd(&sm.hist[dl >> shift], 1);
         }
         __syncthreads();
         locate_bin(sm, r);
@@ -350,18 +358,18 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
         r -= sm.bcast[1];
         n_gt += sm.bcast[1];
         m = sm.bcast[2];
-        lo += uint32_t(bin) << shift;
+        klo += uint32_t(bin) << shift;
         wbits = shift;
         if (shift == 0 || m <= kCand) break;
         shift = max(0, shift - 11);
       }
       if (wbits == 0) {
-        kstar = lo;                          // the bin is one key value
+        kstar = klo;                         // the bin is one key value
         n_eq = m;
       } else {
-        for (int i = tid; i < N; i += kThreads) {
+        for (int i = lo + tid; i < hi; i += kThreads) {
           const uint32_t key = keys_s[i];
-          if (key >= lo && ((key - lo) >> wbits) == 0u) sm.cand[atomicAdd(&sm.bcast[7], 1)] = key;
+          if (key >= klo && ((key - klo) >> wbits) == 0u) sm.cand[atomicAdd(&sm.bcast[7], 1)] = key;
         }
         __syncthreads();
         rank_candidates(sm, m, r);
@@ -376,17 +384,21 @@ __device__ void select_sequence(const ScoreArgs& a, int b, const SelectSmem& sm)
   // ---- selection flags in index order ----
   if (partial && need_eq < n_eq) {
     int eq_cnt = 0;
-    for (int i = c0; i < c1; ++i) eq_cnt += (keys_s[i] == kstar);
+    for (int i = max(c0, lo); i < min(c1, hi); ++i) eq_cnt += (keys_s[i] == kstar);
     int eq_tot;
     int eq_rank = block_exclusive_scan(eq_cnt, sm.scratch, &eq_tot);
     for (int i = c0; i < c1; ++i) {
       const uint32_t key = keys_s[i];
-      bool s = key > kstar;
-      if (key == kstar) { s = eq_rank < need_eq; ++eq_rank; }
+      bool s = true;                                    // forced blocks take no equal-key rank
+      if (i >= lo && i < hi) {
+        s = key > kstar;
+        if (key == kstar) { s = eq_rank < need_eq; ++eq_rank; }
+      }
       flags_s[i] = s ? 1 : 0;
     }
   } else {
-    for (int i = c0; i < c1; ++i) flags_s[i] = (k > 0 && (!partial || keys_s[i] >= kstar)) ? 1 : 0;
+    for (int i = c0; i < c1; ++i)
+      flags_s[i] = (i < lo || i >= hi || (k > 0 && (!partial || keys_s[i] >= kstar))) ? 1 : 0;
   }
   __syncthreads();
 
@@ -868,9 +880,10 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
                               int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
                               int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
                               float* scores_out, void* ws, const kvsel_append_in* app,
-                              int* err, cudaStream_t s) {
+                              int n_sink, int n_recent, int* err, cudaStream_t s) {
   if (p.batch == 0) return cudaSuccess;
   ScoreArgs a;
+  a.n_sink = n_sink; a.n_recent = n_recent;
   a.q = q; a.summaries = summaries; a.seq_lens = seq_lens; a.k_per_seq = k_per_seq;
   a.kv_pages = app ? app->kv_pages : nullptr;
   a.n_pages = app ? app->n_pages : 0;

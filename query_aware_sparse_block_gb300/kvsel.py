@@ -55,6 +55,10 @@ class kvsel_append_in(ctypes.Structure):
                 ("summaries", ctypes.c_void_p), ("open_acc", ctypes.c_void_p)]
 
 
+class kvsel_window(ctypes.Structure):
+    _fields_ = [("n_sink", ctypes.c_int32), ("n_recent", ctypes.c_int32)]
+
+
 class kvsel_kv_src(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("staging_slots", ctypes.c_int32),
                 ("kv_pages", ctypes.c_void_p),
@@ -89,6 +93,10 @@ _SIGS = {
     "kvsel_append_score_topk": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_append_in),
                                      _P, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P, _P, _P, _P,
                                      _P, _P, _P, ctypes.c_size_t, _P]),
+    "kvsel_score_topk_window": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_window),
+                                     ctypes.POINTER(kvsel_append_in), _P, _P, _P, _P, ctypes.c_float,
+                                     ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P,
+                                     ctypes.c_size_t, _P]),
     "kvsel_score_topk_noalloc": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, ctypes.c_float,
                                       ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvsel_noalloc_scratch_bytes": (ctypes.c_size_t, []),
@@ -265,6 +273,30 @@ def kvsel_append_score_topk(p, app: kvsel_append_in, q, seq_lens, k_per_seq, sel
                                          _ptr(dense_flag), _ptr(scores_out), _ptr(ws),
                                          ws.numel() * ws.element_size(), _stream(stream)),
            "kvsel_append_score_topk")
+
+
+def kvsel_score_topk_window(p, n_sink, n_recent, q, summaries, seq_lens, k_per_seq, sel_idx,
+                            n_sel, span_start, span_len, n_spans, ws, app=None, gamma=2.0,
+                            tau_rel=0.0, dense_flag=None, scores_out=None, stream=None):
+    """kvsel_score_topk (or, with ``app``, kvsel_append_score_topk) with the
+    first ``n_sink`` and last ``n_recent`` blocks of every sequence forced
+    into the selection; ``summaries`` may be None when ``app`` is given."""
+    for t, dt, n in ((q, torch.bfloat16, "q"), (summaries, torch.bfloat16, "summaries"),
+                     (seq_lens, torch.int32, "seq_lens"), (k_per_seq, torch.int32, "k_per_seq"),
+                     (sel_idx, torch.int32, "sel_idx"), (n_sel, torch.int32, "n_sel"),
+                     (span_start, torch.int32, "span_start"), (span_len, torch.int32, "span_len"),
+                     (n_spans, torch.int32, "n_spans"), (dense_flag, torch.uint8, "dense_flag"),
+                     (scores_out, torch.float32, "scores_out")):
+        _expect(t, dt, n)
+    win = kvsel_window(int(n_sink), int(n_recent))
+    _check(lib().kvsel_score_topk_window(ctypes.byref(p), ctypes.byref(win),
+                                         ctypes.byref(app) if app is not None else None, _ptr(q),
+                                         _ptr(summaries), _ptr(seq_lens), _ptr(k_per_seq),
+                                         float(gamma), float(tau_rel), _ptr(sel_idx), _ptr(n_sel),
+                                         _ptr(span_start), _ptr(span_len), _ptr(n_spans),
+                                         _ptr(dense_flag), _ptr(scores_out), _ptr(ws),
+                                         ws.numel() * ws.element_size(), _stream(stream)),
+           "kvsel_score_topk_window")
 
 
 def kvsel_score_topk_noalloc(p, q, summaries, seq_lens, k_per_seq, sel_idx, n_sel, span_start,

@@ -78,6 +78,17 @@ class SparseDecoder:
                                   gamma=gamma, tau_rel=tau_rel, dense_flag=self.dense_flag,
                                   scores_out=scores_out, stream=stream)
 
+    def select_window(self, q, summaries, seq_lens, n_sink, n_recent, k_per_seq=None, gamma=2.0,
+                      tau_rel=0.0, scores_out=None, app=None, stream=None):
+        """select() with the first n_sink and last n_recent blocks forced in
+        (kvsel_score_topk_window); ``app`` (kvsel.append_in) folds the
+        token's append into the call as append_select() does."""
+        kp = self.k_per_seq if k_per_seq is None else k_per_seq
+        K.kvsel_score_topk_window(self.p, n_sink, n_recent, q, summaries, seq_lens, kp, self.sel_idx,
+                                  self.n_sel, self.span_start, self.span_len, self.n_spans,
+                                  self.ws_score, app=app, gamma=gamma, tau_rel=tau_rel,
+                                  dense_flag=self.dense_flag, scores_out=scores_out, stream=stream)
+
     def attend(self, q, kv, seq_lens, use_dense_flag=True, out=None, lse=None, out_bf16=None,
                stream=None):
         K.kvsel_sparse_decode(self.p, q, kv, seq_lens, self.sel_idx, self.n_sel,

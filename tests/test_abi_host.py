@@ -32,7 +32,8 @@ def _declared_functions():
 
 def test_header_declares_the_entry_points():
     names = _declared_functions()
-    for n in ("kvsel_build_summaries", "kvsel_score_topk", "kvsel_append_score_topk", "kvsel_merge_spans",
+    for n in ("kvsel_build_summaries", "kvsel_score_topk", "kvsel_append_score_topk",
+              "kvsel_score_topk_window", "kvsel_merge_spans",
               "kvsel_sparse_decode", "kvsel_budget", "kvsel_fetch_spans",
               "kvsel_workspace_size", "kvsel_kv_bytes_per_token", "kvsel_get_error",
               "kvsel_version"):
@@ -133,3 +134,26 @@ def test_entry_points_validate_before_touching_the_device(K):
                                  None, None, None)
     assert rc == K.KVSEL_ERR_INVALID_ARG
     assert b"mode" in L.kvsel_last_error()
+
+
+def test_window_entry_point_validates_before_touching_the_device(K):
+    L = K.lib()
+    good = K.problem(1, 8, 8, 64, 16, 64, 8)
+    bad = K.problem(1, 8, 8, 96, 16, 64, 8)
+
+    def call(p, win, app=None):
+        return L.kvsel_score_topk_window(ctypes.byref(p), ctypes.byref(win) if win is not None else None,
+                                         ctypes.byref(app) if app is not None else None, None, None,
+                                         None, None, 1.0, 0.0, None, None, None, None, None, None,
+                                         None, None, 0, None)
+    assert call(bad, K.kvsel_window(0, 0)) == K.KVSEL_ERR_UNSUPPORTED
+    assert call(good, None) == K.KVSEL_ERR_INVALID_ARG
+    for n_sink, n_recent in ((-1, 0), (0, -2), (5, 4), (9, 0)):     # k_max = 8
+        assert call(good, K.kvsel_window(n_sink, n_recent)) == K.KVSEL_ERR_INVALID_ARG
+        assert b"n_sink" in L.kvsel_last_error()
+    # a valid window reaches the pointer checks
+    assert call(good, K.kvsel_window(4, 4)) == K.KVSEL_ERR_INVALID_ARG
+    assert b"NULL pointer" in L.kvsel_last_error()
+    app = K.kvsel_append_in()
+    assert call(good, K.kvsel_window(1, 1), app) == K.KVSEL_ERR_INVALID_ARG
+    assert b"append" in L.kvsel_last_error()
