@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-offload", action="store_true", help="skip the C4 offload-tier measurement")
     ap.add_argument("--ref-seqs", type=int, default=4, help="sequences per oracle sample")
+    ap.add_argument("--no-window", action="store_true",
+                    help="skip the step with a forced sink block and recency window")
     return ap.parse_args()
 
 
@@ -318,7 +320,8 @@ def run_gpu(args):
     w = C3
     layers = args.layers or w.layers
     n_e2e = 0 if args.no_e2e else max(3, args.steps // 2)
-    total_steps = args.warmup + args.steps + 2 + n_e2e + 2
+    n_win = 0 if args.no_window else max(3, args.steps // 2)
+    total_steps = args.warmup + args.steps + 2 + n_e2e + 2 + n_win + 2
     wb = Workbench(w, layers, total_steps, device)
     K = wb.K
     stream = torch.cuda.Stream(device=device)
@@ -481,6 +484,8 @@ def run_gpu(args):
                    "copies": "pinned host buffers, double-buffered on two copy streams that overlap "
                              "the neighbouring steps' compute"}
 
+        window = run_window(wb, stream, n_win, elapsed_ms / args.steps) if n_win else None
+
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(world, layers, args.steps, elapsed_ms)
     peak, peak_kind = peaks()
@@ -521,6 +526,7 @@ def run_gpu(args):
                   "merge grid",
         "clocks": clk,
         "e2e": e2e,
+        "window": window,
     }
     if world == 1 and not args.no_offload:
         line["offload"] = run_offload(device, K)
@@ -530,6 +536,68 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_window(wb, stream, steps, plain_ms_per_step, n_sink=1, n_recent=4):
+    """The same decode step with the first block and the last four blocks of
+    every sequence forced into the selection (the recency window that the
+    DKV abstract attends exactly beside the Top-k blocks, plus one leading
+    block), Top-k over the blocks between: kvsel_score_topk_window with the
+    token's append folded in, then kvsel_sparse_decode, captured into a CUDA
+    graph and timed as a whole like the main step."""
+    import torch
+
+    from query_aware_sparse_block_gb300.runtime import BoundLayer, SparseDecoder
+
+    w = wb.w
+    dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size, wb.max_blocks,
+                        k_max=wb.k + n_sink + n_recent, device=wb.device)
+    dec.k_per_seq.fill_(wb.k)
+    bound = [BoundLayer(dec, d["x"]["q"], d["x"]["kv_pages"], d["x"]["block_table"], d["summ"],
+                        d["acc"], d["out"], d["lse"], gamma=w.gamma, new_k=d["new_k"],
+                        new_v=d["new_v"], window=(n_sink, n_recent)) for d in wb.layers]
+    plain, wb.bound = wb.bound, bound
+    try:
+        first = wb.step_i
+        acc_snap = [d["acc"].clone() for d in wb.layers]
+
+        def reset_state():
+            wb.pos_buf.copy_(wb.append_pos[first])
+            wb.len_buf.copy_(wb.seq_lens[first])
+            for d, a in zip(wb.layers, acc_snap):
+                d["acc"].copy_(a)
+
+        reset_state()
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        launches0 = wb.K.kvsel_launch_count()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(steps):
+                wb.step(stream, graph=True)
+        launches = wb.K.kvsel_launch_count() - launches0
+        for _ in range(2):              # upload and warm up; untimed
+            graph.replay()
+            stream.synchronize()
+            reset_state()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t0.record(stream)
+        graph.replay()
+        t1.record(stream)
+        stream.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        err = wb.K.kvsel_get_error(stream)
+        if err:
+            raise RuntimeError(f"device error {err} in the window step")
+        n_sel = dec.n_sel.cpu().tolist()
+    finally:
+        wb.bound = plain
+    return {"n_sink": n_sink, "n_recent": n_recent, "k_topk": wb.k, "n_sel": n_sel[0],
+            "value": len(wb.layers) / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": steps,
+            "gpu_launches": int(launches),
+            "vs_plain_step": plain_ms_per_step / ms,
+            "selected_kv_bytes_ratio": (wb.k + n_sink + n_recent) / wb.k}
 
 
 # ------------------------------------------------------------ offload tier ---

@@ -109,11 +109,16 @@ class BoundLayer:
     """
 
     def __init__(self, dec: SparseDecoder, q, kv_pages, block_table, summaries, open_acc,
-                 out, lse, kv=None, gamma=2.0, tau_rel=0.0, new_k=None, new_v=None):
+                 out, lse, kv=None, gamma=2.0, tau_rel=0.0, new_k=None, new_v=None, window=None):
+        """``window`` = (n_sink, n_recent) makes append_select() force those
+        blocks into the selection (kvsel_score_topk_window)."""
         L = K.lib()
         vp = ctypes.c_void_p
         self._fa, self._fs, self._fd = L.kvsel_build_summaries, L.kvsel_score_topk, L.kvsel_sparse_decode
         self._fas = L.kvsel_append_score_topk
+        self._fw = L.kvsel_score_topk_window
+        self._win = K.kvsel_window(*window) if window is not None else None
+        self._win_ref = ctypes.byref(self._win) if window is not None else None
         self.dec = dec
         self.p = ctypes.byref(dec.p)
         self.kv = kv if kv is not None else K.kv_paged(kv_pages, block_table)
@@ -158,7 +163,15 @@ class BoundLayer:
         app.new_k = nk.value if isinstance(nk, ctypes.c_void_p) else nk
         app.new_v = nv.value if isinstance(nv, ctypes.c_void_p) else nv
         s = self.sel
-        rc = self._fas(self.p, self._app_ref, q_ptr if q_ptr is not None else self.q, seq_lens_ptr,
+        qp = q_ptr if q_ptr is not None else self.q
+        if self._win is not None:
+            rc = self._fw(self.p, self._win_ref, self._app_ref, qp, None, seq_lens_ptr, self.kps,
+                          self.gamma, self.tau, s[0], s[1], s[2], s[3], s[4], s[5], None,
+                          self.ws1, self.ws1n, stream_ptr)
+            if rc:
+                K._check(rc, "kvsel_score_topk_window")
+            return
+        rc = self._fas(self.p, self._app_ref, qp, seq_lens_ptr,
                        self.kps, self.gamma, self.tau, s[0], s[1], s[2], s[3], s[4], s[5], None,
                        self.ws1, self.ws1n, stream_ptr)
         if rc:
