@@ -371,3 +371,60 @@ def decode_seq(q_bits, k_bits, v_bits, T: int, B: int, k: int, scale: float,
     blocks = np.arange(N) if dense else sel
     out, lse = attend(q_bits, k_bits, v_bits, tokens_of_blocks(blocks, T, B), scale)
     return SeqStep(scores, sel, ss, sl, bool(dense), out, lse)
+
+
+# ---------------------------------------------------------------------------
+# [Offload] "NOSA": selection is local across consecutive decode steps, so
+# blocks fetched in one step are kept on the GPU and reused in the next, and
+# an eviction policy bounds the blocks fetched from host memory.
+# ---------------------------------------------------------------------------
+
+class BlockCache:
+    """GPU-resident copies of host-tier blocks of one sequence, ``slots`` of them.
+
+    Readings where the pages are silent:
+      * Eviction is least recently selected first: a slot's stamp is the last
+        step in which its block was selected (-1 while empty); the victims are
+        the slots not selected in this step with the smallest (stamp, slot
+        index), so empty slots go first, in slot order.
+      * The misses of a step, taken in ascending block order, fill the victims
+        in that order.
+      * Full blocks never change; the block holding the last token changes as
+        tokens are appended, so when it is selected its copy is fetched again
+        even on a hit (into the slot it already holds).
+    """
+
+    def __init__(self, slots: int):
+        self.slots = int(slots)
+        self.block_in = [-1] * self.slots
+        self.last_use = [-1] * self.slots
+        self.slot_of: dict[int, int] = {}
+
+    def step(self, sel, step: int, last_block: int):
+        """Serve one step's ascending selection; returns (fetch jobs, hits)
+        with each job (block, slot): the misses in ascending block order, then
+        the refresh of the last block if it was a hit."""
+        sel = [int(n) for n in sel]
+        assert len(sel) <= self.slots
+        hits, misses, refresh = [], [], []
+        for n in sel:
+            s = self.slot_of.get(n)
+            if s is None:
+                misses.append(n)
+            else:
+                hits.append(n)
+                self.last_use[s] = step
+                if n == last_block:
+                    refresh.append((n, s))
+        free = [s for s in range(self.slots) if self.last_use[s] != step]
+        free.sort(key=lambda s: (self.last_use[s], s))
+        jobs = []
+        for n, s in zip(misses, free):
+            old = self.block_in[s]
+            if old >= 0:
+                del self.slot_of[old]
+            self.block_in[s] = n
+            self.slot_of[n] = s
+            self.last_use[s] = step
+            jobs.append((n, s))
+        return jobs + refresh, hits

@@ -507,3 +507,81 @@ def test_c0_step_runs_and_is_self_consistent():
     r = o.decode_seq(bits(x["q"][0]), kb, vb, w.seq_len, w.block_size, w.topk, 1 / 8)
     assert len(r.sel) == w.topk and r.span_len.sum() == w.topk
     assert np.all(np.isfinite(r.out)) and np.all(np.isfinite(r.lse))
+
+
+# ------------------------------------------------------------ block cache ---
+
+def test_block_cache_hand_example(golden_dir):
+    c = o.BlockCache(3)
+    for r in _rows(os.path.join(golden_dir, "block_cache_hand_example.txt")):
+        step, sel, last, jobs, hits, blk, use = (p.strip() for p in r.split("|"))
+        got_jobs, got_hits = c.step([int(v) for v in sel.split()], int(step), int(last))
+        want_jobs = [] if jobs == "-" else [tuple(int(x) for x in j.split(":")) for j in jobs.split()]
+        assert got_jobs == want_jobs, step
+        assert got_hits == ([] if hits == "-" else [int(v) for v in hits.split()])
+        assert c.block_in == [int(v) for v in blk.split()]
+        assert c.last_use == [int(v) for v in use.split()]
+
+
+def _random_selections(g, steps, N, k, locality):
+    sel = np.sort(g.choice(N, size=k, replace=False))
+    out = []
+    for _ in range(steps):
+        keep = sel[g.random(k) < locality]
+        rest = np.setdiff1d(np.arange(N), keep)
+        sel = np.sort(np.concatenate([keep, g.choice(rest, size=k - len(keep), replace=False)]))
+        out.append(sel)
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_block_cache_invariants_and_lru_order_from_history(seed):
+    g = np.random.default_rng(seed)
+    N, k = 40, int(g.integers(3, 9))
+    slots = k + int(g.integers(0, 7))
+    c = o.BlockCache(slots)
+    last_sel = {}                       # block -> last step it was selected (raw history)
+    resident_prev = set()
+    for step, sel in enumerate(_random_selections(g, 60, N, k, 0.7)):
+        last = int(g.integers(N - 3, N))
+        jobs, hits = c.step(sel, step, last)
+        sel_set = set(sel.tolist())
+        resident = {b for b in c.block_in if b >= 0}
+        # every selected block is resident; hits were resident before
+        assert sel_set <= resident and set(hits) <= resident_prev
+        assert len(resident) <= slots
+        # block_in and slot_of are inverse maps
+        assert all(c.block_in[s] == b for b, s in c.slot_of.items())
+        assert len(c.slot_of) == len(resident)
+        misses = sorted(sel_set - set(hits))
+        assert [n for n, _ in jobs[:len(misses)]] == misses
+        assert jobs[len(misses):] == ([(last, c.slot_of[last])] if last in hits else [])
+        # LRU from the raw history: no evicted block was selected later than a
+        # block that stayed without being selected in this step
+        evicted = resident_prev - resident
+        kept_idle = (resident & resident_prev) - sel_set
+        if evicted and kept_idle:
+            assert max(last_sel[b] for b in evicted) <= min(last_sel[b] for b in kept_idle)
+        for b in sel_set:
+            last_sel[b] = step
+        resident_prev = resident
+
+
+def test_block_cache_special_cases():
+    # the same selection again: nothing to fetch but the refreshed last block
+    c = o.BlockCache(8)
+    assert len(c.step([1, 3, 9], 0, 9)[0]) == 3
+    assert c.step([1, 3, 9], 1, 9) == ([(9, c.slot_of[9])], [1, 3, 9])
+    assert c.step([1, 3, 9], 2, 12) == ([], [1, 3, 9])
+    # disjoint selections with slots == k: every block is fetched and the
+    # evicted ones are exactly the previous step's
+    c = o.BlockCache(4)
+    prev = None
+    for step in range(5):
+        sel = list(range(4 * step, 4 * step + 4))
+        jobs, hits = c.step(sel, step, 100)
+        assert hits == [] and [n for n, _ in jobs] == sel
+        assert sorted(b for b in c.block_in) == sel
+        if prev is not None:
+            assert not set(prev) & set(c.block_in)
+        prev = sel
