@@ -356,6 +356,63 @@ KVSEL_API int kvsel_fetch_spans(const kvsel_problem* p, const kvsel_kv_src* kv, 
                       const int32_t* n_spans, const uint8_t* dense_flag,
                       kvsel_stream_t stream);
 
+/* A GPU-resident cache of host-tier blocks: `slots` pool pages per sequence
+ * and the state that maps blocks to them. Every pointer is a device pointer
+ * owned by the caller. */
+typedef struct kvsel_block_cache {
+  int32_t slots;        /* pool pages per sequence; k_max <= slots <= 4096 */
+  kvsel_bf16* pool;     /* [batch][slots][one KV page] bf16 (page b * slots + s) */
+  int32_t* page_of;     /* [batch][max_blocks]: pool page holding block n, or -1 */
+  int32_t* block_in;    /* [batch][slots]: block held by slot s, or -1 */
+  int32_t* last_use;    /* [batch][slots]: last step slot s was selected, -1 = empty */
+} kvsel_block_cache;
+
+/*
+ * kvsel_cache_reset -- empties the cache: every page_of, block_in and
+ * last_use entry becomes -1 (three cudaMemsetAsync on `stream`). Call it once
+ * before the first kvsel_cache_fetch, and whenever the host tier is replaced.
+ */
+KVSEL_API int kvsel_cache_reset(const kvsel_problem* p, const kvsel_block_cache* cache,
+                                kvsel_stream_t stream);
+
+/*
+ * kvsel_cache_fetch -- the offload tier's recovery copy with cross-step reuse
+ * ("KV cache offloading", section "NOSA": block selection is local across
+ * consecutive decode steps, so blocks fetched in one step are kept on the GPU
+ * and reused in the next, and an eviction policy bounds the blocks fetched
+ * from host memory). Two kernels on `stream`:
+ *  - per sequence b, every selected block sel_idx[b][0..n_sel[b]) that the
+ *    cache holds is a hit and its slot is stamped with `step`; the misses, in
+ *    ascending block order, take the slots not selected in this step with the
+ *    smallest (last_use, slot) -- least recently selected first, empty slots
+ *    before any -- evicting the blocks they held;
+ *  - every miss is copied from host_kv (pinned, device-mapped; layout of the
+ *    host tier) into its pool page, and so is the block holding the last
+ *    token (N_b - 1) when it was a hit, since appends change it.
+ * n_fetched[b] (nullable, device int32) receives the number of blocks copied.
+ * Afterwards every selected block is resident: attend with
+ * kvsel_sparse_decode on kind KVSEL_KV_PAGED with kv_pages = cache->pool,
+ * block_table = cache->page_of, n_pages = batch * slots, and dense_flag =
+ * NULL (a sequence whose gamma flag is set needs every block: serve it with
+ * KVSEL_KV_HOST instead; the cache is not updated for it).
+ *
+ * step: >= 0 and different from the step of the previous call on this cache
+ * (a step counter). slots >= k_max guarantees a free slot for every miss.
+ * ws: kvsel_workspace_size(p, KVSEL_WS_CACHE_FETCH) bytes (job lists; no
+ * initial contents required). fetch_ctas: CTAs of the copy kernel (0 = one
+ * per SM). Errors: INVALID_ARG (NULL or misaligned pointer, slots outside
+ * [k_max, 4096], step < 0, host_kv not device-mapped pinned memory),
+ * WORKSPACE, UNSUPPORTED, CUDA; device BOUNDS for a selection that is not
+ * strictly ascending, an index outside [0, min(N_b, host_blocks)) (not
+ * served) or an inconsistent cache state (the block is fetched again).
+ */
+KVSEL_API int kvsel_cache_fetch(const kvsel_problem* p, const kvsel_block_cache* cache,
+                                const kvsel_bf16* host_kv, int32_t host_blocks,
+                                const int32_t* seq_lens, const int32_t* sel_idx,
+                                const int32_t* n_sel, int32_t step, int32_t* n_fetched,
+                                int32_t fetch_ctas, void* ws, size_t ws_bytes,
+                                kvsel_stream_t stream);
+
 /* Budget inputs ("SparPR KV cache recovery on a consumer GPU", paragraph
  * "Dynamic budget control"). */
 typedef struct kvsel_budget_in {
@@ -392,7 +449,7 @@ typedef struct kvsel_budget_out {
  */
 KVSEL_API int kvsel_budget(const kvsel_budget_in* in, kvsel_budget_out* out);
 
-enum kvsel_ws_kind { KVSEL_WS_SCORE_TOPK = 0, KVSEL_WS_SPARSE_DECODE = 1 };
+enum kvsel_ws_kind { KVSEL_WS_SCORE_TOPK = 0, KVSEL_WS_SPARSE_DECODE = 1, KVSEL_WS_CACHE_FETCH = 2 };
 
 /* Workspace bytes an entry point needs for problem p (0 on bad input). */
 KVSEL_API size_t kvsel_workspace_size(const kvsel_problem* p, int which);

@@ -159,6 +159,7 @@ size_t kvsel_workspace_size(const kvsel_problem* p, int which) {
   if (check_problem(p) != KVSEL_OK) return 0;
   if (which == KVSEL_WS_SCORE_TOPK) return score_topk_ws_bytes(*p);
   if (which == KVSEL_WS_SPARSE_DECODE) return sparse_decode_ws_bytes(*p);
+  if (which == KVSEL_WS_CACHE_FETCH) return cache_fetch_ws_bytes(*p);
   return 0;
 }
 
@@ -402,6 +403,75 @@ static int check_host_kv(const kvsel_problem* p, const kvsel_kv_src* kv, const v
   if (rows >= (int64_t(1) << 31))
     return fail(KVSEL_ERR_UNSUPPORTED, "host tier: staging larger than 2^31 rows");
   return KVSEL_OK;
+}
+
+static int check_cache(const char* who, const kvsel_problem* p, const kvsel_block_cache* c) {
+  char msg[200];
+  if (!c || !c->pool || !c->page_of || !c->block_in || !c->last_use) {
+    std::snprintf(msg, sizeof msg, "%s: cache and its pool, page_of, block_in, last_use required", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (c->slots < p->k_max || c->slots > 4096) {
+    std::snprintf(msg, sizeof msg, "%s: slots must be in [k_max, 4096]", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (!aligned16(c->pool) || !aligned4(c->page_of) || !aligned4(c->block_in) || !aligned4(c->last_use)) {
+    std::snprintf(msg, sizeof msg, "%s: misaligned cache pointer", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (int64_t(p->batch) * c->slots * p->n_kvheads * 2 * p->block_size >= (int64_t(1) << 31)) {
+    std::snprintf(msg, sizeof msg, "%s: pool larger than 2^31 rows", who);
+    return fail(KVSEL_ERR_UNSUPPORTED, msg);
+  }
+  return KVSEL_OK;
+}
+
+int kvsel_cache_reset(const kvsel_problem* p, const kvsel_block_cache* c, kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  r = check_cache("cache_reset", p, c);
+  if (r) return r;
+  if (p->batch == 0) return KVSEL_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // all-ones bytes are -1 in every int32 entry: no block cached, every slot empty
+  cudaError_t e = cudaMemsetAsync(c->page_of, 0xFF, size_t(p->batch) * p->max_blocks * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->block_in, 0xFF, size_t(p->batch) * c->slots * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->last_use, 0xFF, size_t(p->batch) * c->slots * 4, s);
+  return cuda_status(e, "cache_reset");
+}
+
+int kvsel_cache_fetch(const kvsel_problem* p, const kvsel_block_cache* c, const kvsel_bf16* host_kv,
+                      int32_t host_blocks, const int32_t* seq_lens, const int32_t* sel_idx,
+                      const int32_t* n_sel, int32_t step, int32_t* n_fetched, int32_t fetch_ctas,
+                      void* ws, size_t ws_bytes, kvsel_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return r;
+  r = check_cache("cache_fetch", p, c);
+  if (r) return r;
+  if (p->batch == 0) return KVSEL_OK;
+  if (!host_kv || host_blocks <= 0 || !seq_lens || !sel_idx || !n_sel)
+    return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: host_kv, host_blocks, seq_lens, sel_idx, n_sel required");
+  if (step < 0) return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: step must be >= 0");
+  if (!aligned16(host_kv) || !aligned4(seq_lens) || !aligned4(sel_idx) || !aligned4(n_sel) ||
+      (n_fetched && !aligned4(n_fetched)))
+    return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: misaligned pointer");
+  if (!ws || ws_bytes < cache_fetch_ws_bytes(*p) || !aligned16(ws))
+    return fail(KVSEL_ERR_WORKSPACE, "cache_fetch: workspace missing, small or misaligned");
+  if (cache_update_smem_bytes(*p, c->slots) > size_t(max_smem_optin()))
+    return fail(KVSEL_ERR_UNSUPPORTED, "cache_fetch: slots and k_max exceed shared memory");
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host_kv) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: host_kv is not known to CUDA (pin it)");
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr)
+    return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: host_kv is not device-mapped pinned memory");
+  int* ew = device_error_word();
+  if (!ew) return fail(KVSEL_ERR_CUDA, "cache_fetch: no CUDA device");
+  return cuda_status(launch_cache_fetch(*p, *c, static_cast<const kvsel_bf16*>(at.devicePointer),
+                                        host_blocks, seq_lens, sel_idx, n_sel, step, n_fetched, ws,
+                                        fetch_ctas, ew, reinterpret_cast<cudaStream_t>(stream)),
+                     "cache_fetch launch");
 }
 
 int kvsel_fetch_spans(const kvsel_problem* p, const kvsel_kv_src* kv, const int32_t* seq_lens,

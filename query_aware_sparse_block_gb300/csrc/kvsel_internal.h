@@ -59,4 +59,13 @@ cudaError_t launch_fetch_spans(const kvsel_problem& p, const kvsel_kv_src& kv,
                                const int32_t* span_len, const int32_t* n_spans,
                                const uint8_t* dense_flag, int* err, cudaStream_t s);
 
+// ---- GPU-resident block cache of the host tier (block_cache.cu) ----
+size_t cache_fetch_ws_bytes(const kvsel_problem& p);
+size_t cache_update_smem_bytes(const kvsel_problem& p, int slots);
+cudaError_t launch_cache_fetch(const kvsel_problem& p, const kvsel_block_cache& c,
+                               const kvsel_bf16* host_kv, int host_blocks,
+                               const int32_t* seq_lens, const int32_t* sel_idx,
+                               const int32_t* n_sel, int step, int32_t* n_fetched, void* ws,
+                               int fetch_ctas, int* err, cudaStream_t s);
+
 }  // namespace kvsel

@@ -31,6 +31,7 @@ KVSEL_KV_STAGED = 1
 KVSEL_KV_HOST = 2
 KVSEL_WS_SCORE_TOPK = 0
 KVSEL_WS_SPARSE_DECODE = 1
+KVSEL_WS_CACHE_FETCH = 2
 
 _STATUS = {1: "INVALID_ARG", 2: "CUDA", 3: "BOUNDS", 4: "TIMEOUT", 5: "UNSUPPORTED", 6: "WORKSPACE"}
 
@@ -57,6 +58,11 @@ class kvsel_append_in(ctypes.Structure):
 
 class kvsel_window(ctypes.Structure):
     _fields_ = [("n_sink", ctypes.c_int32), ("n_recent", ctypes.c_int32)]
+
+
+class kvsel_block_cache(ctypes.Structure):
+    _fields_ = [("slots", ctypes.c_int32), ("pool", ctypes.c_void_p), ("page_of", ctypes.c_void_p),
+                ("block_in", ctypes.c_void_p), ("last_use", ctypes.c_void_p)]
 
 
 class kvsel_kv_src(ctypes.Structure):
@@ -106,6 +112,10 @@ _SIGS = {
                                  ctypes.c_size_t, _P]),
     "kvsel_fetch_spans": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_kv_src), _P, _P, _P,
                                _P, _P, _P]),
+    "kvsel_cache_reset": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_block_cache), _P]),
+    "kvsel_cache_fetch": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_block_cache), _P,
+                               ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P,
+                               ctypes.c_size_t, _P]),
     "kvsel_budget": (_I, [ctypes.POINTER(kvsel_budget_in), ctypes.POINTER(kvsel_budget_out)]),
     "kvsel_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kvsel_problem), _I]),
     "kvsel_kv_bytes_per_token": (ctypes.c_int64, [ctypes.c_int32] * 4),
@@ -316,6 +326,35 @@ def kvsel_score_topk_noalloc(p, q, summaries, seq_lens, k_per_seq, sel_idx, n_se
                                           _ptr(span_len), _ptr(n_spans), _ptr(dense_flag),
                                           _ptr(scores_out), _stream(stream)),
            "kvsel_score_topk_noalloc")
+
+
+def block_cache(slots, pool, page_of, block_in, last_use) -> kvsel_block_cache:
+    """The cache descriptor (the tensors stay owned by the caller)."""
+    for t, dt, n in ((pool, torch.bfloat16, "pool"), (page_of, torch.int32, "page_of"),
+                     (block_in, torch.int32, "block_in"), (last_use, torch.int32, "last_use")):
+        _expect(t, dt, n)
+    return kvsel_block_cache(int(slots), _ptr(pool), _ptr(page_of), _ptr(block_in), _ptr(last_use))
+
+
+def kvsel_cache_reset(p, cache: kvsel_block_cache, stream=None):
+    _check(lib().kvsel_cache_reset(ctypes.byref(p), ctypes.byref(cache), _stream(stream)),
+           "kvsel_cache_reset")
+
+
+def kvsel_cache_fetch(p, cache: kvsel_block_cache, host_kv, host_blocks, seq_lens, sel_idx, n_sel,
+                      step, ws, n_fetched=None, fetch_ctas=0, stream=None):
+    """Serve a step's selection from the block cache, copying the misses (and
+    the refreshed last block) from the pinned host tier."""
+    if host_kv.is_cuda or not host_kv.is_pinned():
+        raise TypeError("host_kv must be a pinned host tensor")
+    for t, dt, n in ((seq_lens, torch.int32, "seq_lens"), (sel_idx, torch.int32, "sel_idx"),
+                     (n_sel, torch.int32, "n_sel"), (n_fetched, torch.int32, "n_fetched")):
+        _expect(t, dt, n)
+    _check(lib().kvsel_cache_fetch(ctypes.byref(p), ctypes.byref(cache), _ptr(host_kv), int(host_blocks),
+                                   _ptr(seq_lens), _ptr(sel_idx), _ptr(n_sel), int(step),
+                                   _ptr(n_fetched), int(fetch_ctas), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)),
+           "kvsel_cache_fetch")
 
 
 def kvsel_merge_spans(p, sel_idx, n_sel, span_start, span_len, n_spans, stream=None):

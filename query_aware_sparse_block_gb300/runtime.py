@@ -193,3 +193,37 @@ class BoundLayer:
                       self.ws2, self.ws2n, stream_ptr)
         if rc:
             K._check(rc, "kvsel_sparse_decode")
+
+
+class HostBlockCache:
+    """Device buffers of a GPU-resident cache of host-tier blocks
+    (kvsel_cache_fetch): ``slots`` pool pages per sequence, the block/slot
+    maps and a step counter. After fetch(), ``kv`` is the paged view of the
+    pool that kvsel_sparse_decode reads (dense flag off)."""
+
+    def __init__(self, dec: SparseDecoder, slots, page_shape):
+        p = dec.p
+        self.p, self.slots, self.device = p, int(slots), dec.device
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.pool = torch.empty((p.batch * self.slots,) + tuple(page_shape), dtype=torch.bfloat16,
+                                device=self.device)
+        self.page_of = torch.empty((p.batch, p.max_blocks), **i32)
+        self.block_in = torch.empty((p.batch, self.slots), **i32)
+        self.last_use = torch.empty((p.batch, self.slots), **i32)
+        self.n_fetched = torch.zeros((p.batch,), **i32)
+        self.ws = torch.zeros((K.kvsel_workspace_size(p, K.KVSEL_WS_CACHE_FETCH),), dtype=torch.uint8,
+                              device=self.device)
+        self.desc = K.block_cache(self.slots, self.pool, self.page_of, self.block_in, self.last_use)
+        self.kv = K.kv_paged(self.pool, self.page_of)
+        self.step = 0
+        self.reset()
+
+    def reset(self, stream=None):
+        K.kvsel_cache_reset(self.p, self.desc, stream=stream)
+        self.step = 0
+
+    def fetch(self, host_kv, host_blocks, seq_lens, sel_idx, n_sel, fetch_ctas=0, stream=None):
+        K.kvsel_cache_fetch(self.p, self.desc, host_kv, host_blocks, seq_lens, sel_idx, n_sel,
+                            self.step, self.ws, n_fetched=self.n_fetched, fetch_ctas=fetch_ctas,
+                            stream=stream)
+        self.step += 1

@@ -33,7 +33,7 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ("kvsel_build_summaries", "kvsel_score_topk", "kvsel_append_score_topk",
-              "kvsel_score_topk_window", "kvsel_merge_spans",
+              "kvsel_score_topk_window", "kvsel_merge_spans", "kvsel_cache_reset", "kvsel_cache_fetch",
               "kvsel_sparse_decode", "kvsel_budget", "kvsel_fetch_spans",
               "kvsel_workspace_size", "kvsel_kv_bytes_per_token", "kvsel_get_error",
               "kvsel_version"):
@@ -157,3 +157,26 @@ def test_window_entry_point_validates_before_touching_the_device(K):
     app = K.kvsel_append_in()
     assert call(good, K.kvsel_window(1, 1), app) == K.KVSEL_ERR_INVALID_ARG
     assert b"append" in L.kvsel_last_error()
+
+
+def test_cache_entry_points_validate_before_touching_the_device(K):
+    L = K.lib()
+    p = K.problem(2, 8, 8, 64, 16, 64, 8)
+    assert K.kvsel_workspace_size(p, K.KVSEL_WS_CACHE_FETCH) >= 2 * 9 * 8 + 8
+    c = K.kvsel_block_cache()
+    assert L.kvsel_cache_reset(ctypes.byref(p), None, None) == K.KVSEL_ERR_INVALID_ARG
+    assert L.kvsel_cache_reset(ctypes.byref(p), ctypes.byref(c), None) == K.KVSEL_ERR_INVALID_ARG
+    c.pool, c.page_of, c.block_in, c.last_use = 16, 16, 16, 16
+    for slots in (7, 4097):                  # below k_max, above the limit
+        c.slots = slots
+        assert L.kvsel_cache_reset(ctypes.byref(p), ctypes.byref(c), None) == K.KVSEL_ERR_INVALID_ARG
+        assert b"slots" in L.kvsel_last_error()
+    c.slots = 8
+
+    def fetch(host, step, ws, nws):
+        return L.kvsel_cache_fetch(ctypes.byref(p), ctypes.byref(c), host, 64, 4, 4, 4, step, None, 0,
+                                   ws, nws, None)
+    assert fetch(None, 0, 16, 4096) == K.KVSEL_ERR_INVALID_ARG
+    assert fetch(16, -1, 16, 4096) == K.KVSEL_ERR_INVALID_ARG
+    assert b"step" in L.kvsel_last_error()
+    assert fetch(16, 0, None, 0) == K.KVSEL_ERR_WORKSPACE
