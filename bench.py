@@ -682,9 +682,68 @@ def run_offload(device, K, reps=5):
             "frac_of_h2d_copy": link_bytes / fetch_s / 1e9 / h2d_gbs,
             "fetch_plus_attend_us": decode_s * 1e6}
         del staging
+    res["block_cache"] = run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs,
+                                         res[f"keep_{w.keep_floor:g}"]["fetch_plus_attend_us"])
     del host
     torch.cuda.empty_cache()
     return res
+
+
+def run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs, uncached_us, steps=8,
+                    rho=0.95):
+    """The floor selection (k = 102 of 2048 blocks) served through the GPU
+    block cache (kvsel_cache_fetch, 2k slots per sequence) over consecutive
+    steps whose queries drift, q_s = rho q_(s-1) + sqrt(1 - rho^2) e_s with
+    e_s ~ N(0, 1): per warm step the blocks that crossed the link, the hit
+    rate, the fetch time and rate against the measured copy rate, and select
+    + fetch + attend against the uncached gather + attend."""
+    import torch
+    from query_aware_sparse_block_gb300.runtime import HostBlockCache, SparseDecoder
+
+    N = w.n_blocks
+    k = w.k_for(w.keep_floor)
+    page_bytes = int(np.prod(page)) * 2
+    dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size, x["max_blocks"],
+                        k_max=k, device=device)
+    dec.k_per_seq.fill_(k)
+    cache = HostBlockCache(dec, 2 * k, page)
+    g = torch.Generator(device=device).manual_seed(4242)
+    q = x["q"].float()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    rows = []
+    for step in range(steps):
+        if step:
+            q = rho * q + math.sqrt(1 - rho * rho) * torch.randn(q.shape, generator=g, device=device)
+        qb = q.to(torch.bfloat16)
+        torch.cuda.synchronize()
+        ev[0].record()
+        dec.select(qb, summ, x["seq_lens"], gamma=w.gamma)
+        ev[1].record()
+        cache.fetch(host, N, x["seq_lens"], dec.sel_idx, dec.n_sel)
+        ev[2].record()
+        dec.attend(qb, cache.kv, x["seq_lens"], use_dense_flag=False)
+        ev[3].record()
+        torch.cuda.synchronize()
+        if int(dec.dense_flag.sum()):
+            raise RuntimeError("a sequence went dense at the keep floor")
+        fetched = int(cache.n_fetched.sum())
+        rows.append((fetched, ev[1].elapsed_time(ev[2]) * 1e3, ev[0].elapsed_time(ev[3]) * 1e3))
+    err = K.kvsel_get_error()
+    if err:
+        raise RuntimeError(f"device error {err} in the block-cache measurement")
+    warm = rows[1:]
+    blocks = statistics.mean(r[0] for r in warm)
+    fetch_us = statistics.mean(r[1] for r in warm)
+    step_us = statistics.mean(r[2] for r in warm)
+    link = blocks * page_bytes
+    del cache
+    torch.cuda.empty_cache()
+    return {"k": k, "slots": 2 * k, "rho": rho, "steps": steps,
+            "cold_step_blocks": rows[0][0], "blocks_per_step": blocks,
+            "hit_rate": 1.0 - blocks / (w.batch * k), "link_bytes_per_step": link,
+            "fetch_us": fetch_us, "fetch_gbs": link / (fetch_us / 1e6) / 1e9,
+            "frac_of_h2d_copy": link / (fetch_us / 1e6) / 1e9 / h2d_gbs,
+            "select_fetch_attend_us": step_us, "uncached_fetch_plus_attend_us": uncached_us}
 
 
 # ------------------------------------------------------ oracle (reference) ---
