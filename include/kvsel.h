@@ -297,7 +297,8 @@ KVSEL_API size_t kvsel_noalloc_scratch_bytes(void);
 enum kvsel_kv_kind {
   KVSEL_KV_PAGED = 0,  /* K/V pages in device memory + block table */
   KVSEL_KV_STAGED = 1, /* selected blocks already in a device staging buffer */
-  KVSEL_KV_HOST = 2    /* full K/V in pinned host memory: fetch the spans, then attend */
+  KVSEL_KV_HOST = 2,   /* full K/V in pinned host memory: fetch the spans, then attend */
+  KVSEL_KV_HOST_DIRECT = 3 /* full K/V in pinned host memory, read by the attention kernel itself */
 };
 
 /* Where the K/V of the attended blocks come from. */
@@ -308,8 +309,8 @@ typedef struct kvsel_kv_src {
   const int32_t* block_table;     /* PAGED */
   int64_t n_pages;                /* PAGED: pages in kv_pages */
   kvsel_bf16* staging;            /* STAGED/HOST: device staging buffer */
-  const kvsel_bf16* host_kv;      /* HOST: pinned host tier (device-mapped) */
-  int32_t host_blocks;            /* HOST: block stride of the host tier per sequence */
+  const kvsel_bf16* host_kv;      /* HOST, HOST_DIRECT: pinned host tier (device-mapped) */
+  int32_t host_blocks;            /* HOST, HOST_DIRECT: block stride of the host tier per sequence */
   int32_t fetch_ctas;             /* HOST: CTAs of the gather kernel (0 = one per SM) */
 } kvsel_kv_src;
 
@@ -329,7 +330,13 @@ typedef struct kvsel_kv_src {
  * kv: see kvsel_kv_src. STAGED: the o-th attended block of b is staging slot
  * o (block n when dense). HOST: the selected spans (or all blocks when dense)
  * are first gathered from host_kv into staging on `stream` (see
- * kvsel_fetch_spans), then treated as STAGED.
+ * kvsel_fetch_spans), then treated as STAGED. HOST_DIRECT: the attention
+ * kernel reads each attended block straight from host_kv (block n of b at
+ * [b][n] of the host tier) through unified virtual addressing with 16-byte
+ * asynchronous copies into shared memory, so no staging buffer and no
+ * second pass over device memory is needed ("KV cache offloading", sections
+ * "NOSA" and "SparDA": kernels that read host memory directly); a block
+ * index >= host_blocks latches BOUNDS and is skipped.
  * out: device fp32 output; out_bf16: optional bf16 copy; lse: device fp32.
  * ws: kvsel_workspace_size(p, KVSEL_WS_SPARSE_DECODE) bytes.
  */

@@ -545,6 +545,21 @@ int kvsel_sparse_decode(const kvsel_problem* p, const kvsel_bf16* q, const kvsel
     if (int64_t(p->batch) * kv->staging_slots * 2 * p->n_kvheads * p->block_size >= (int64_t(1) << 31))
       return fail(KVSEL_ERR_UNSUPPORTED, "sparse_decode: staging larger than 2^31 rows");
     src.kind = KVSEL_KV_STAGED;
+  } else if (kv->kind == KVSEL_KV_HOST_DIRECT) {
+    if (!kv->host_kv || kv->host_blocks <= 0 || !aligned16(kv->host_kv))
+      return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: host_direct needs an aligned host_kv and host_blocks");
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, kv->host_kv) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: host_kv is not known to CUDA (pin it)");
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr)
+      return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: host_kv is not device-mapped pinned memory");
+    if (!aligned16(at.devicePointer))
+      return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: misaligned host_kv mapping");
+    if (int64_t(p->batch) * kv->host_blocks * p->n_kvheads >= (int64_t(1) << 31))
+      return fail(KVSEL_ERR_UNSUPPORTED, "sparse_decode: host tier larger than 2^31 tiles");
+    src.host_kv = static_cast<const kvsel_bf16*>(at.devicePointer);
   } else {
     return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: unknown kv kind");
   }

@@ -217,6 +217,18 @@ __device__ __forceinline__ uint4 ld_sys_v4(const void* p) {
   return v;
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only); the source may be
+// host-mapped memory.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(src) : "memory");
+}
+
+// The mbarrier tracks every cp.async this thread issued before: its pending
+// count goes up by one now and comes down when those copies have landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void stg_stream(void* p, uint4 v) {
   asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
                "r"(v.z), "r"(v.w)

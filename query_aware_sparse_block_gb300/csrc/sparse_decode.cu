@@ -62,7 +62,8 @@ inline int heads_per_group(int B, int Hkv) {
 }
 
 struct DecodeArgs {
-  const kvsel_bf16* kv_base;  // PAGED: KV pages; STAGED: staging (the same page layout)
+  const kvsel_bf16* kv_base;  // PAGED: KV pages; STAGED: staging; HOST_DIRECT: the host tier
+                              // (device-mapped); all in the same page layout
   const kvsel_bf16* q;
   const int32_t* seq_lens;
   const int32_t* sel_idx;
@@ -72,6 +73,7 @@ struct DecodeArgs {
   int64_t n_pages;
   int kind;
   int slots;
+  int host_blocks;     // HOST_DIRECT: block stride of the host tier per sequence
   float scale_log2;
   float* out;
   kvsel_bf16* out_bf16;
@@ -123,6 +125,9 @@ __device__ void tile_info(const DecodeArgs& a, const int* base_s, const int* tle
     int64_t page = ok ? a.block_table[int64_t(b) * a.max_blocks + n] : 0;
     if (page < 0 || page >= a.n_pages) { ok = false; page = 0; }
     unit = int(page * a.n_groups + hg);
+  } else if (a.kind == KVSEL_KV_HOST_DIRECT) {
+    if (n >= a.host_blocks) ok = false;
+    unit = ok ? int((int64_t(b) * a.host_blocks + n) * a.n_groups + hg) : 0;
   } else {
     int64_t slot = o;
     if (slot >= a.slots) { ok = false; slot = 0; }
@@ -295,6 +300,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
     unsigned char* dst = tiles + size_t(slot_idx(m)) * tile_bytes;
     bulk_load_hint(dst, a.kv_base + int64_t(unit) * 2 * plane_elems, uint32_t(tile_bytes), bar, pol);
   };
+  // From host-mapped memory the tile arrives by 16-byte cp.async reads of the
+  // whole warp instead of one bulk copy (the same bytes land in the same
+  // place); each lane's copies arrive on the slot's barrier when they have
+  // landed, and lane 0's ordinary arrival completes the count of one.
+  const bool host_direct = a.kind == KVSEL_KV_HOST_DIRECT;
+  auto issue_warp = [&](int m, int unit) {   // whole warp
+    uint64_t* bar = slot_bar(m);
+    const uint32_t dst = smem_u32(tiles + size_t(slot_idx(m)) * tile_bytes);
+    const unsigned char* src =
+        reinterpret_cast<const unsigned char*>(a.kv_base + int64_t(unit) * 2 * plane_elems);
+    for (int off = lane * 16; off < tile_bytes; off += 32 * 16) cp_async_16(dst + off, src + off);
+    cp_async_mbar_arrive(bar);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  };
   if (active) {
     load_batch(0, cur_rk, cur_cnt);
     load_batch(32, nxt_rk, nxt_cnt);
@@ -303,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
     for (int m = 0; m < min(S, LR); ++m) {
       int rk, cnt;
       tile_desc(m, rk, cnt);
-      if (lane == 0) issue(m, rk);
+      if (host_direct) issue_warp(m, rk);
+      else if (lane == 0) issue(m, rk);
     }
   }
   bool dead = false;
@@ -362,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
           dead = true;
           if (lane == 0) latch_error(a.err, KVSEL_ERR_TIMEOUT);
         }
+        if (host_direct) dead = __any_sync(0xffffffffu, dead);   // the refill is warp-wide
         const int cnt = t_cnt - slice * 16;    // valid tokens in this warp's 16 rows
         const uint32_t st = tiles_base + uint32_t(slot_idx(m_cur)) * uint32_t(tile_bytes);
         if (!dead && cnt > 0) {
@@ -494,7 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
         if (last && !dead && m_cur + S < LR) {
           int rk, cnt2;
           tile_desc(m_cur + S, rk, cnt2);
-          if (lane == 0) {
+          if (host_direct) {
+            issue_warp(m_cur + S, rk);
+          } else if (lane == 0) {
             fence_proxy_async();
             issue(m_cur + S, rk);
           }
@@ -539,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   if (dead && lane == 0 && task == 0)
     for (int m = m_cur; m < min(LR, m_cur + S); ++m)
       (void)mbar_wait_bounded(slot_bar(m), uint32_t((m / S) & 1));
+  if (host_direct) asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's copies
 }
 
 // One warp per output row (sequence b, query head h): log-sum-exp merge of the
@@ -679,8 +704,9 @@ cudaError_t launch_sparse_decode(const kvsel_problem& p, const kvsel_bf16* q,
   DecodeArgs a{};
   a.q = q; a.seq_lens = seq_lens; a.sel_idx = sel_idx; a.n_sel = n_sel; a.dense_flag = dense_flag;
   a.block_table = kv.block_table; a.n_pages = kv.n_pages;
-  a.kind = (kv.kind == KVSEL_KV_PAGED) ? KVSEL_KV_PAGED : KVSEL_KV_STAGED;
+  a.kind = (kv.kind == KVSEL_KV_PAGED || kv.kind == KVSEL_KV_HOST_DIRECT) ? kv.kind : KVSEL_KV_STAGED;
   a.slots = kv.staging_slots;
+  a.host_blocks = kv.host_blocks;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = out; a.out_bf16 = out_bf16; a.lse = lse;
   char* w = static_cast<char*>(ws);
@@ -692,7 +718,8 @@ cudaError_t launch_sparse_decode(const kvsel_problem& p, const kvsel_bf16* q,
   a.batch = p.batch; a.Hq = p.n_qheads; a.Hkv = p.n_kvheads; a.G = p.n_qheads / p.n_kvheads;
   a.B = p.block_size; a.max_blocks = p.max_blocks; a.k_max = p.k_max;
   const int D = p.head_dim;
-  a.kv_base = a.kind == KVSEL_KV_PAGED ? kv.kv_pages : kv.staging;
+  a.kv_base = a.kind == KVSEL_KV_PAGED ? kv.kv_pages
+              : a.kind == KVSEL_KV_HOST_DIRECT ? kv.host_kv : kv.staging;
   const int Bs = p.block_size;
   if (D == 128 && Bs == 16) return a.G <= 8 ? launch_t<128, 16, 1>(p, a, s) : launch_t<128, 16, 2>(p, a, s);
   if (D == 128 && Bs == 32) return a.G <= 8 ? launch_t<128, 32, 1>(p, a, s) : launch_t<128, 32, 2>(p, a, s);

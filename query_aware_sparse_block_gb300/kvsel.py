@@ -29,6 +29,7 @@ KVSEL_SUMMARY_APPEND = 1
 KVSEL_KV_PAGED = 0
 KVSEL_KV_STAGED = 1
 KVSEL_KV_HOST = 2
+KVSEL_KV_HOST_DIRECT = 3
 KVSEL_WS_SCORE_TOPK = 0
 KVSEL_WS_SPARSE_DECODE = 1
 KVSEL_WS_CACHE_FETCH = 2
@@ -393,6 +394,17 @@ def kv_host(host_kv, host_blocks, staging, slots, fetch_ctas=0) -> kvsel_kv_src:
     s.kind = KVSEL_KV_HOST
     s.host_kv, s.host_blocks = _ptr(host_kv), int(host_blocks)
     s.staging, s.staging_slots, s.fetch_ctas = _ptr(staging), int(slots), int(fetch_ctas)
+    return s
+
+
+def kv_host_direct(host_kv, host_blocks) -> kvsel_kv_src:
+    """The host tier read by the attention kernel itself (no staging)."""
+    if host_kv.is_cuda or not host_kv.is_pinned():
+        raise TypeError("host_kv must be a pinned host tensor")
+    _expect(host_kv, torch.bfloat16, "host_kv", cuda=False)
+    s = kvsel_kv_src()
+    s.kind = KVSEL_KV_HOST_DIRECT
+    s.host_kv, s.host_blocks = _ptr(host_kv), int(host_blocks)
     return s
 
 
