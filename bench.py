@@ -673,6 +673,9 @@ def run_offload(device, K, reps=5):
                                                     dec.span_len, dec.n_spans, dec.dense_flag), reps)
         link_bytes = int(dec.n_sel.sum()) * page_bytes
         decode_s = timed(lambda: dec.attend(x["q"], kv, x["seq_lens"]), reps)
+        # the attention kernel reading the host tier itself (no staging pass)
+        kv_direct = K.kv_host_direct(host, N)
+        direct_s = timed(lambda: dec.attend(x["q"], kv_direct, x["seq_lens"]), reps)
         err = K.kvsel_get_error()
         if err:
             raise RuntimeError(f"device error {err} in the offload measurement")
@@ -680,7 +683,10 @@ def run_offload(device, K, reps=5):
             "k": k, "dense_sequences": n_dense, "link_bytes_per_step": link_bytes,
             "fetch_us": fetch_s * 1e6, "fetch_gbs": link_bytes / fetch_s / 1e9,
             "frac_of_h2d_copy": link_bytes / fetch_s / 1e9 / h2d_gbs,
-            "fetch_plus_attend_us": decode_s * 1e6}
+            "fetch_plus_attend_us": decode_s * 1e6,
+            "host_direct_attend_us": direct_s * 1e6,
+            "host_direct_gbs": link_bytes / direct_s / 1e9,
+            "host_direct_frac_of_h2d_copy": link_bytes / direct_s / 1e9 / h2d_gbs}
         del staging
     res["block_cache"] = run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs,
                                          res[f"keep_{w.keep_floor:g}"]["fetch_plus_attend_us"])
@@ -710,16 +716,21 @@ def run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs, uncached_
     g = torch.Generator(device=device).manual_seed(4242)
     q = x["q"].float()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-    rows = []
+    rows, host_us = [], []
     for step in range(steps):
         if step:
             q = rho * q + math.sqrt(1 - rho * rho) * torch.randn(q.shape, generator=g, device=device)
         qb = q.to(torch.bfloat16)
         torch.cuda.synchronize()
+        # a bounded device-side delay (about 1 ms) while the host enqueues the
+        # whole step, so that the events time the GPU and not the host calls
+        torch.cuda._sleep(2_000_000)
         ev[0].record()
         dec.select(qb, summ, x["seq_lens"], gamma=w.gamma)
         ev[1].record()
+        h0 = time.perf_counter()
         cache.fetch(host, N, x["seq_lens"], dec.sel_idx, dec.n_sel)
+        host_us.append((time.perf_counter() - h0) * 1e6)
         ev[2].record()
         dec.attend(qb, cache.kv, x["seq_lens"], use_dense_flag=False)
         ev[3].record()
@@ -743,7 +754,9 @@ def run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs, uncached_
             "hit_rate": 1.0 - blocks / (w.batch * k), "link_bytes_per_step": link,
             "fetch_us": fetch_us, "fetch_gbs": link / (fetch_us / 1e6) / 1e9,
             "frac_of_h2d_copy": link / (fetch_us / 1e6) / 1e9 / h2d_gbs,
-            "select_fetch_attend_us": step_us, "uncached_fetch_plus_attend_us": uncached_us}
+            "select_fetch_attend_us": step_us, "uncached_fetch_plus_attend_us": uncached_us,
+            "fetch_call_host_us": statistics.median(host_us),
+            "per_step": [[r[0], round(r[1], 1)] for r in rows]}
 
 
 # ------------------------------------------------------ oracle (reference) ---
