@@ -690,9 +690,48 @@ def run_offload(device, K, reps=5):
         del staging
     res["block_cache"] = run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs,
                                          res[f"keep_{w.keep_floor:g}"]["fetch_plus_attend_us"])
+    res["copy_unit_sweep"] = run_copy_unit_sweep(device, K, host, timed, h2d_gbs)
     del host
     torch.cuda.empty_cache()
     return res
+
+
+def run_copy_unit_sweep(device, K, host, timed, h2d_gbs, reps=5):
+    """Does the size of one copied unit matter on this link? The span gather
+    on 64 sequences whose selection is every 16th block (spans of one block,
+    so every unit is one page) for pages of 16, 32, 64 and 256 KiB (block
+    sizes 16 / 32 / 64 with 2 KV heads, 64 with 8), d 128, over the first
+    GiB of the pinned host tier viewed in each layout."""
+    import torch
+    from query_aware_sparse_block_gb300 import kvsel as KK
+
+    out = []
+    flat = host.view(-1)[: 1 << 29]                 # 1 GiB of bf16
+    for B, Hkv in ((16, 2), (32, 2), (64, 2), (64, 8)):
+        page = (Hkv, 2, 2, B, 64)
+        page_elems = int(np.prod(page))
+        batch = 64
+        N = flat.numel() // (batch * page_elems)
+        k = N // 16
+        tier = flat[: batch * N * page_elems].view((batch, N) + page)
+        p = KK.problem(batch, 4 * Hkv, Hkv, 128, B, N, k)
+        i32 = dict(dtype=torch.int32, device=device)
+        starts = (torch.arange(k, **i32) * 16).repeat(batch, 1).contiguous()
+        lens = torch.ones((batch, k), **i32)
+        n_spans = torch.full((batch,), k, **i32)
+        seq_lens = torch.full((batch,), N * B, **i32)
+        staging = torch.empty((batch, k) + page, dtype=torch.bfloat16, device=device)
+        kv = KK.kv_host(tier, N, staging, k)
+        t = timed(lambda: KK.kvsel_fetch_spans(p, kv, seq_lens, starts, lens, n_spans, None), reps)
+        nbytes = batch * k * page_elems * 2
+        out.append({"page_kib": page_elems * 2 // 1024, "units_per_step": batch * k,
+                    "bytes_per_step": nbytes, "fetch_us": t * 1e6, "gbs": nbytes / t / 1e9,
+                    "frac_of_h2d_copy": nbytes / t / 1e9 / h2d_gbs})
+        del staging
+    err = K.kvsel_get_error()
+    if err:
+        raise RuntimeError(f"device error {err} in the copy-unit sweep")
+    return out
 
 
 def run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs, uncached_us, steps=8,
