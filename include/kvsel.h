@@ -471,6 +471,18 @@ KVSEL_API int64_t kvsel_kv_bytes_per_token(int32_t layers, int32_t kv_heads, int
  * `stream` (a synchronising call). Returns KVSEL_OK or the first device error. */
 KVSEL_API int kvsel_get_error(kvsel_stream_t stream);
 
+/*
+ * kvsel_selftest_wait_timeout -- exercises, on the current device, the path
+ * that every bounded device wait of the library takes when it runs out: one
+ * thread waits on an mbarrier phase that nothing completes; after the wait
+ * limit (2 s) the wait gives up, the kernel latches KVSEL_ERR_TIMEOUT into
+ * the error word and returns, and the context stays usable. The pages
+ * describe no such call; it lets a deployment check its failure detection
+ * without faulting or hanging the GPU. Enqueued on `stream`; the next
+ * kvsel_get_error() returns KVSEL_ERR_TIMEOUT (and clears it).
+ */
+KVSEL_API int kvsel_selftest_wait_timeout(kvsel_stream_t stream);
+
 /* Kernel launches made by this library since load (host-side counter). */
 KVSEL_API uint64_t kvsel_launch_count(void);
 

@@ -199,6 +199,33 @@ int kvsel_budget(const kvsel_budget_in* in, kvsel_budget_out* out) {
   return KVSEL_OK;
 }
 
+}  // extern "C"
+
+namespace kvsel {
+namespace {
+// One thread waits, with the library's bounded wait, on a barrier phase that
+// nothing completes: the wait must give up and the kernel report it.
+__global__ void wait_selftest_kernel(int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait_bounded(&bar, 0u)) latch_error(err, KVSEL_ERR_TIMEOUT);
+  }
+}
+}  // namespace
+}  // namespace kvsel
+
+extern "C" {
+
+int kvsel_selftest_wait_timeout(kvsel_stream_t stream) {
+  int* ew = device_error_word();
+  if (!ew) return fail(KVSEL_ERR_CUDA, "selftest_wait_timeout: no CUDA device");
+  wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ew);
+  count_launch();
+  return cuda_status(cudaGetLastError(), "selftest_wait_timeout launch");
+}
+
 int kvsel_get_error(kvsel_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int r = cuda_status(cudaStreamSynchronize(s), "kvsel_get_error: stream sync");

@@ -121,6 +121,7 @@ _SIGS = {
     "kvsel_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kvsel_problem), _I]),
     "kvsel_kv_bytes_per_token": (ctypes.c_int64, [ctypes.c_int32] * 4),
     "kvsel_get_error": (_I, [_P]),
+    "kvsel_selftest_wait_timeout": (_I, [_P]),
     "kvsel_launch_count": (ctypes.c_uint64, []),
     "kvsel_last_error": (ctypes.c_char_p, []),
     "kvsel_version": (ctypes.c_char_p, []),
@@ -212,6 +213,11 @@ def kvsel_budget(block_size, kv_heads, head_dim, elem_bytes, hidden, n_blocks, h
     o = kvsel_budget_out()
     _check(lib().kvsel_budget(ctypes.byref(i), ctypes.byref(o)), "kvsel_budget")
     return o
+
+
+def kvsel_selftest_wait_timeout(stream=None):
+    """Enqueue the bounded-wait self-test; kvsel_get_error() then returns KVSEL_ERR_TIMEOUT."""
+    _check(lib().kvsel_selftest_wait_timeout(_stream(stream)), "kvsel_selftest_wait_timeout")
 
 
 def kvsel_get_error(stream=None) -> int:

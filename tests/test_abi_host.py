@@ -34,6 +34,7 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ("kvsel_build_summaries", "kvsel_score_topk", "kvsel_append_score_topk",
               "kvsel_score_topk_window", "kvsel_merge_spans", "kvsel_cache_reset", "kvsel_cache_fetch",
+              "kvsel_selftest_wait_timeout",
               "kvsel_sparse_decode", "kvsel_budget", "kvsel_fetch_spans",
               "kvsel_workspace_size", "kvsel_kv_bytes_per_token", "kvsel_get_error",
               "kvsel_version"):
