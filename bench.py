@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-offload", action="store_true", help="skip the C4 offload-tier measurement")
     ap.add_argument("--ref-seqs", type=int, default=4, help="sequences per oracle sample")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-layer step on the other workload shapes")
     ap.add_argument("--no-window", action="store_true",
                     help="skip the step with a forced sink block and recency window")
     return ap.parse_args()
@@ -485,6 +487,9 @@ def run_gpu(args):
                              "the neighbouring steps' compute"}
 
         window = run_window(wb, stream, n_win, elapsed_ms / args.steps) if n_win else None
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = run_configs(device)
 
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(world, layers, args.steps, elapsed_ms)
@@ -508,13 +513,16 @@ def run_gpu(args):
                    "l2": "inputs larger than L2 (distinct buffers per layer, no flush)"},
         "roofline": {"kernel": "sparse_decode", "bound": "hbm", "achieved": dec_gbs, "peak": peak,
                      "unit": "GB/s", "frac": dec_gbs / peak, "peak_kind": peak_kind,
+                     "frac_of_nominal": dec_gbs / NOMINAL_HBM_GBS,
                      "traffic": traffic, "bytes_per_launch": dec_bytes,
                      "avg_launch_us": dec_avg_ms * 1e3},
         "kernels": {
             "score_topk": {"bytes_per_launch": sc_bytes, "avg_launch_us": sc_avg_ms * 1e3,
-                           "achieved_gbs": sc_gbs, "frac": sc_gbs / peak},
+                           "achieved_gbs": sc_gbs, "frac": sc_gbs / peak,
+                           "frac_of_nominal": sc_gbs / NOMINAL_HBM_GBS},
             "sparse_decode": {"bytes_per_launch": dec_bytes, "avg_launch_us": dec_avg_ms * 1e3,
-                              "achieved_gbs": dec_gbs, "frac": dec_gbs / peak},
+                              "achieved_gbs": dec_gbs, "frac": dec_gbs / peak,
+                              "frac_of_nominal": dec_gbs / NOMINAL_HBM_GBS},
         },
         "gpu_launches": int(launches),
         "host_capture_ms_per_step": host_ms,
@@ -527,6 +535,7 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": e2e,
         "window": window,
+        "configs": configs,
     }
     if world == 1 and not args.no_offload:
         line["offload"] = run_offload(device, K)
@@ -536,6 +545,74 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+NOMINAL_HBM_GBS = 7900.0    # GB300 HBM3e, nominal
+
+
+def run_configs(device, passes=4, min_pass_bytes=400e6):
+    """The decode step (score + Top-k, then sparse decode; no append) on the
+    other workload shapes: tiny MHA (C0), OPT-6.7B-shaped MHA at keep 50 % and
+    10 % (C1), MiniCPM4.1-8B-shaped GQA at 128K tokens (C2). Enough distinct
+    layers are resident that one pass over them moves more than three times
+    the L2; a CUDA graph of `passes` passes is timed with events. Reports
+    layer-steps/s and the step's algorithmic bytes (summaries, q, selected K/V,
+    outputs) per second against the measured and the nominal HBM bandwidth."""
+    import ctypes
+
+    import torch
+
+    from query_aware_sparse_block_gb300.runtime import BoundLayer, SparseDecoder
+    from workloads import C0, C1, C2
+    from workloads.generate import generate_layer
+
+    peak, _ = peaks()
+    out = []
+    for w in (C0, C1, C2):
+        for k in w.ks:
+            N = w.n_blocks
+            per_layer = (w.batch * N * w.n_kvheads * w.head_dim * 2 + w.batch * w.n_qheads * w.head_dim * 2
+                         + w.batch * k * w.n_kvheads * 2 * w.block_size * w.head_dim * 2
+                         + w.batch * w.n_qheads * (w.head_dim + 1) * 4)
+            nl = max(2, int(math.ceil(min_pass_bytes / per_layer)))
+            dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size, N, k_max=k,
+                                device=device)
+            dec.k_per_seq.fill_(k)
+            layers, keep = [], []
+            for l in range(nl):
+                x = generate_layer(w, l, device=device, perm=False)
+                summ, acc = dec.new_summaries()
+                dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
+                keep.append((x, summ, acc))
+                layers.append(BoundLayer(dec, x["q"], x["kv_pages"], x["block_table"], summ, acc,
+                                         dec.out, dec.lse, gamma=2.0))
+            lens = ctypes.c_void_p(keep[0][0]["seq_lens"].data_ptr())
+            s = torch.cuda.Stream(device=device)
+            sp = ctypes.c_void_p(s.cuda_stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(passes):
+                    for bl in layers:
+                        bl.select(lens, sp)
+                        bl.attend(lens, sp)
+            with torch.cuda.stream(s):
+                g.replay()
+                s.synchronize()
+                t0 = torch.cuda.Event(enable_timing=True)
+                t1 = torch.cuda.Event(enable_timing=True)
+                t0.record(s)
+                g.replay()
+                t1.record(s)
+                s.synchronize()
+            us = t0.elapsed_time(t1) * 1e3 / (passes * nl)
+            gbs = per_layer / (us / 1e6) / 1e9
+            out.append({"workload": w.name, "k": k, "layers_resident": nl, "us_per_layer_step": us,
+                        "layer_steps_per_s": 1e6 / us, "bytes_per_layer_step": per_layer,
+                        "achieved_gbs": gbs, "frac": gbs / peak, "frac_of_nominal": gbs / NOMINAL_HBM_GBS})
+            del g, layers, keep, dec
+            torch.cuda.empty_cache()
+    return out
 
 
 def run_window(wb, stream, steps, plain_ms_per_step, n_sink=1, n_recent=4):
