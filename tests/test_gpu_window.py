@@ -97,6 +97,7 @@ SMALL = [
     ("gqa4_d128_B32_sink3", C3.scaled(batch=3, seq_len=2000, drift_amp=0.0, layers=1), [2000, 100, 1999], 6, 3, 0),
     ("gqa4_d128_B32_sink2_recent4", C3.scaled(batch=3, seq_len=3000, drift_amp=0.0, layers=1), [3000, 150, 2500], 20, 2, 4),
     ("gqa16_d128_B64_recent8", C2.scaled(batch=2, seq_len=9000, layers=1), [9000, 4097], 5, 1, 8),
+    ("k0_window_only_and_empty", C0.scaled(batch=3, seq_len=320), [320, 0, 40], 0, 1, 3),
 ]
 
 
@@ -104,7 +105,7 @@ SMALL = [
 def test_window_small_cases_elementwise(K, name, w, lens, k, n_sink, n_recent):
     x = to_dev(generate_layer(w, 0, seq_lens=lens), "cuda:0")
     mb = x["max_blocks"]
-    dec = _decoder(w, mb, k_max=k + n_sink + n_recent)
+    dec = _decoder(w, mb, k_max=max(1, k + n_sink + n_recent))
     summ, acc = dec.new_summaries()
     dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
     dec.k_per_seq.fill_(k)
