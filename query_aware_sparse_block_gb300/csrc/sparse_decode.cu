@@ -566,23 +566,33 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   if (host_direct) asm volatile("cp.async.wait_all;" ::: "memory");   // this thread's copies
 }
 
-// One warp per output row (sequence b, query head h): log-sum-exp merge of the
-// states every warp stored for the row's segment. Lane l owns channels
-// [l * D/32, (l + 1) * D/32); up to 16 states are read at once, every lane
-// loading each state's (max, sum) and its own channel slice, so a chunk of
-// states costs one round trip to L2. Launched as a programmatic dependent of
-// the decode kernel: it can be resident early and waits for the decode grid's
-// completion before it reads anything that grid wrote.
-template <int D, int WPH>
+// Log-sum-exp merge, per output row (sequence b, query head h), of the states
+// every decode warp stored for the row's segment: one warp per row (MW = 1,
+// four rows per CTA), or, when rows have many states, one CTA of four warps
+// per row (MW = 4). Warp w takes every MW-th chunk of 16 states; lane l owns channels
+// [l * D/32, (l + 1) * D/32), and every lane loads each state's (max, sum) and
+// its own channel slice, so a chunk costs one round trip to L2. With MW = 4 the
+// four partial results are then merged through shared memory by warp 0. A long
+// sequence attended by few blocks per CTA (one sequence of 131072 tokens, say)
+// spreads its segment over many CTAs and so gives a row many states; four
+// warps read them in a quarter of the round trips. Launched as a programmatic
+// dependent of the decode kernel: it can be resident early and waits for the
+// decode grid's completion before it reads anything that grid wrote.
+template <int D, int WPH, int MW>
 __global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a) {
   constexpr int kCPL = D / 32;            // channels per lane
   constexpr int kChunk = 16;              // states in flight per lane
   constexpr int kPerCta = kRings * WPH;   // warps of one CTA holding a head
+  static_assert(MW == 1 || MW == 4, "one or four warps per row");
+  constexpr int kMW = MW;                 // warps sharing one row's states
+  constexpr int kRowsPerCta = 4 / MW;
   using vec_t = typename std::conditional<kCPL == 4, float4, float2>::type;
+  __shared__ float ml_s[4][2];
+  __shared__ vec_t o_s[3][32];
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int lane = threadIdx.x & 31;
-  const int64_t row = int64_t(blockIdx.x) * 4 + (threadIdx.x >> 5);
-  if (row >= int64_t(a.batch) * a.Hq) return;
+  const int lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) % kMW;
+  const int64_t row = int64_t(blockIdx.x) * kRowsPerCta + (threadIdx.x >> 5) / kMW;
+  if (row >= int64_t(a.batch) * a.Hq) return;   // uniform in a CTA when kMW == 4
   const int b = int(row / a.Hq), hq = int(row % a.Hq);
   const int G = a.G, j = hq / G, r = hq % G;
   const int hg = j / a.hpg, h_local = j % a.hpg;
@@ -600,7 +610,7 @@ __global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a) {
   float acc[kCPL];
 #pragma unroll
   for (int u = 0; u < kCPL; ++u) acc[u] = 0.f;
-  for (int i0 = 0; i0 < NP; i0 += kChunk) {
+  for (int i0 = wq * kChunk; i0 < NP; i0 += kMW * kChunk) {   // every kMW-th chunk
     float mi[kChunk], li[kChunk];
     vec_t oi[kChunk];
 #pragma unroll
@@ -633,6 +643,45 @@ __global__ void __launch_bounds__(128) merge_rows_kernel(DecodeArgs a) {
       }
     }
     M = mc;
+  }
+  // the kMW partial states of the row, merged by warp 0
+  if constexpr (kMW > 1) {
+  if (lane == 0) {
+    ml_s[wq][0] = M;
+    ml_s[wq][1] = L;
+  }
+  if (wq > 0) {
+    vec_t v;
+    float* vp = reinterpret_cast<float*>(&v);
+#pragma unroll
+    for (int u = 0; u < kCPL; ++u) vp[u] = acc[u];
+    o_s[wq - 1][lane] = v;
+  }
+  __syncthreads();
+  if (wq > 0) return;
+  {
+    float mx = M;
+#pragma unroll
+    for (int w = 1; w < kMW; ++w) mx = fmaxf(mx, ml_s[w][0]);
+    if (mx != -INFINITY) {
+      const float r0 = M == -INFINITY ? 0.f : ex2(M - mx);
+      L *= r0;
+#pragma unroll
+      for (int u = 0; u < kCPL; ++u) acc[u] *= r0;
+#pragma unroll
+      for (int w = 1; w < kMW; ++w) {
+        const float mw = ml_s[w][0];
+        if (mw == -INFINITY) continue;
+        const float rw = ex2(mw - mx);
+        L += rw * ml_s[w][1];
+        const vec_t v = o_s[w - 1][lane];
+        const float* ov = reinterpret_cast<const float*>(&v);
+#pragma unroll
+        for (int u = 0; u < kCPL; ++u) acc[u] += rw * ov[u];
+      }
+      M = mx;
+    }
+  }
   }
   vec_t res;
   float* rv = reinterpret_cast<float*>(&res);
@@ -672,9 +721,19 @@ cudaError_t launch_t(const kvsel_problem& p, const DecodeArgs& a0, cudaStream_t 
   e = launch_pdl(kfn, dim3(grid), dim3(kThreads), smem, s, a);
   count_launch();
   if (e != cudaSuccess) return e;
-  // the row merge, as a programmatic dependent of the decode grid
-  const unsigned merge_grid = unsigned((int64_t(p.batch) * p.n_qheads + 3) / 4);
-  e = launch_pdl(merge_rows_kernel<D, B / 16>, dim3(merge_grid), dim3(128), 0, s, a);
+  // The row merge, as a programmatic dependent of the decode grid. A row has
+  // (CTAs its segment spans) x kRings x B/16 states; bound the span with the
+  // decode's own split applied to k_max blocks per sequence, and give rows
+  // with more than four chunks of states four warps each.
+  const int64_t rows = int64_t(p.batch) * p.n_qheads;
+  const int64_t total_max = int64_t(p.batch) * a.n_groups * p.k_max;
+  const int64_t ctas = std::min<int64_t>(sm_count(), std::max<int64_t>(1, (total_max + kMinTilesPerCta - 1) / kMinTilesPerCta));
+  const int64_t per_cta = std::max<int64_t>(1, total_max / ctas);
+  const int64_t span = (p.k_max + per_cta - 1) / per_cta + 1;
+  if (span * kRings * (B / 16) > 64)
+    e = launch_pdl(merge_rows_kernel<D, B / 16, 4>, dim3(unsigned(rows)), dim3(128), 0, s, a);
+  else
+    e = launch_pdl(merge_rows_kernel<D, B / 16, 1>, dim3(unsigned((rows + 3) / 4)), dim3(128), 0, s, a);
   count_launch();
   return e;
 }
