@@ -181,3 +181,20 @@ def test_cache_entry_points_validate_before_touching_the_device(K):
     assert fetch(16, -1, 16, 4096) == K.KVSEL_ERR_INVALID_ARG
     assert b"step" in L.kvsel_last_error()
     assert fetch(16, 0, None, 0) == K.KVSEL_ERR_WORKSPACE
+
+
+def test_header_compiles_as_c_and_the_library_links_from_c(K, tmp_path):
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path / "abi_from_c")
+    libdir = os.path.dirname(K.LIB_PATH)
+    cmd = [gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           os.path.join(ROOT, "tests", "abi_from_c.c"), "-L", libdir, "-lkvsel",
+           "-Wl,-rpath," + libdir, "-o", exe]
+    subprocess.run(cmd, check=True, capture_output=True, text=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.strip().endswith("all ok")
