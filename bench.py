@@ -490,6 +490,7 @@ def run_gpu(args):
     configs = None
     if world == 1 and not args.no_configs:
         configs = run_configs(device)
+        configs.append(run_summary_build(device))
 
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(world, layers, args.steps, elapsed_ms)
@@ -548,6 +549,43 @@ def run_gpu(args):
 
 
 NOMINAL_HBM_GBS = 7900.0    # GB300 HBM3e, nominal
+
+
+def run_summary_build(device, reps=3):
+    """The FULL summary build (prefill; off the per-step path) on one layer of
+    the Qwen3-4B-shaped batch (1 GiB of keys) and on the MiniCPM-shaped
+    sequence (64 MiB): key bytes read per second and fp64 additions per second
+    (one per key element; the sum is sequential in token order by definition)."""
+    import torch
+
+    from query_aware_sparse_block_gb300.runtime import SparseDecoder
+    from workloads import C2, C3
+    from workloads.generate import generate_layer
+
+    peak, _ = peaks()
+    res = {"kind": "summary_build_full"}
+    for w in (C3, C2):
+        x = generate_layer(w, 0, device=device, perm=False)
+        dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size, x["max_blocks"],
+                            k_max=1, device=device)
+        summ, acc = dec.new_summaries()
+        dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(reps):
+            dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
+        t1.record()
+        torch.cuda.synchronize()
+        us = t0.elapsed_time(t1) * 1e3 / reps
+        elems = w.batch * w.seq_len * w.n_kvheads * w.head_dim
+        res[w.name] = {"us": us, "key_bytes": elems * 2, "key_gbs": elems * 2 / (us / 1e6) / 1e9,
+                       "frac_of_hbm": elems * 2 / (us / 1e6) / 1e9 / peak,
+                       "fp64_add_per_s": elems / (us / 1e6)}
+        del x, dec, summ, acc
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_configs(device, passes=4, min_pass_bytes=400e6):

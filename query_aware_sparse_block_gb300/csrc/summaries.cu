@@ -15,8 +15,10 @@ namespace {
 
 constexpr int kThreads = 128;
 
-// One CTA per (block n, sequence b). Threads own 8-channel column vectors of
-// one KV head and walk the block's tokens in order (pages in the tiled layout).
+// A CTA takes `bpc` consecutive blocks of sequence b (as many as its threads
+// cover: one thread per 8-channel column vector of one KV head, so a block of
+// few heads shares the CTA with its neighbours). Each thread walks its
+// column's tokens in order (pages in the tiled layout).
 __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
     const kvsel_bf16* __restrict__ kv_pages, int64_t n_pages, const int32_t* __restrict__ block_table,
     const int32_t* __restrict__ seq_lens, kvsel_bf16* __restrict__ summaries,
@@ -24,29 +26,34 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
   // a kernel launched after this one with programmatic serialization may
   // become resident now; it waits for this grid's completion before reading
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int n = blockIdx.x;
+  const int vec_per_head = d / 8;
+  const int n_vec = H * vec_per_head;
+  const int bpc = n_vec >= kThreads ? 1 : kThreads / n_vec;     // blocks per CTA
+  const int sub = n_vec >= kThreads ? 0 : int(threadIdx.x) / n_vec;
+  if (sub >= bpc) return;                                        // threads past the last block
+  const int lt = n_vec >= kThreads ? int(threadIdx.x) : int(threadIdx.x) % n_vec;
+  const int step = n_vec >= kThreads ? kThreads : n_vec;
+  const int n = blockIdx.x * bpc + sub;
   const int b = blockIdx.y;
   int T = seq_lens[b];
   if (T < 0 || T > max_blocks * B) {
-    if (n == 0 && threadIdx.x == 0) latch_error(err, KVSEL_ERR_BOUNDS);
+    if (n == 0 && lt == 0) latch_error(err, KVSEL_ERR_BOUNDS);
     T = T < 0 ? 0 : max_blocks * B;
   }
   const int N = (T + B - 1) / B;
-  const int vec_per_head = d / 8;
-  const int n_vec = H * vec_per_head;
   if (N == 0) {
     if (n == 0)
-      for (int i = threadIdx.x; i < H * d; i += blockDim.x) open_acc[int64_t(b) * H * d + i] = 0.0;
+      for (int i = lt; i < H * d; i += step) open_acc[int64_t(b) * H * d + i] = 0.0;
     return;
   }
   if (n >= N) return;
   const int64_t page = block_table[int64_t(b) * max_blocks + n];
   if (page < 0 || page >= n_pages) {
-    if (threadIdx.x == 0) latch_error(err, KVSEL_ERR_BOUNDS);
+    if (lt == 0) latch_error(err, KVSEL_ERR_BOUNDS);
     return;
   }
   const int cnt = min(B, T - n * B);
-  for (int v = threadIdx.x; v < n_vec; v += blockDim.x) {
+  for (int v = lt; v < n_vec; v += step) {
     const int j = v / vec_per_head;
     const int c0 = (v % vec_per_head) * 8;
     const kvsel_bf16* tile = kv_pages + (page * H + j) * 2 * int64_t(B) * d;
@@ -146,7 +153,9 @@ cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16*
                                    cudaStream_t s) {
   if (p.batch == 0) return cudaSuccess;
   if (mode == KVSEL_SUMMARY_FULL) {
-    dim3 grid(p.max_blocks, p.batch);
+    const int n_vec = p.n_kvheads * p.head_dim / 8;
+    const int bpc = n_vec >= kThreads ? 1 : kThreads / n_vec;
+    dim3 grid((p.max_blocks + bpc - 1) / bpc, p.batch);
     summaries_full_kernel<<<grid, kThreads, 0, s>>>(kv_pages, n_pages, block_table, seq_lens,
                                                     summaries, open_acc, p.n_kvheads, p.head_dim,
                                                     p.block_size, p.max_blocks, err);

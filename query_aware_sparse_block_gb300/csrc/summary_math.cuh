@@ -31,11 +31,30 @@ __device__ __forceinline__ uint16_t f64_to_bf16_rne(double x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// The fp64 value of a bf16 bit pattern h (low 16 bits), exactly. A normal
+// number, an infinity or a NaN is re-encoded with integer operations (exponent
+// rebiased from 127 to 1023, the 7 fraction bits moved to the top of the 52),
+// so the conversion does not occupy the fp64 pipe, which this part runs at a
+// small fraction of its fp32 rate; +-0 is built the same way and only a
+// subnormal (exponent field 0, fraction non-zero) takes the fp32 -> fp64
+// conversion instruction.
+__device__ __forceinline__ double bf16_to_f64(uint32_t h) {
+  const uint32_t e = (h >> 7) & 0xFFu;
+  const uint64_t sign = uint64_t(h & 0x8000u) << 48;
+  if (e == 0u) {
+    if ((h & 0x7Fu) == 0u) return __longlong_as_double(static_cast<long long>(sign));
+    return static_cast<double>(__uint_as_float(h << 16));
+  }
+  const uint64_t ex = e == 0xFFu ? 0x7FFull : uint64_t(e + (1023u - 127u));
+  const uint64_t man = uint64_t(h & 0x7Fu) << 45;
+  return __longlong_as_double(static_cast<long long>(sign | (ex << 52) | man));
+}
+
 __device__ __forceinline__ void unpack8(const uint4& v, double (&x)[8]) {
-  x[0] = bf16lo(v.x); x[1] = bf16hi(v.x);
-  x[2] = bf16lo(v.y); x[3] = bf16hi(v.y);
-  x[4] = bf16lo(v.z); x[5] = bf16hi(v.z);
-  x[6] = bf16lo(v.w); x[7] = bf16hi(v.w);
+  x[0] = bf16_to_f64(v.x & 0xFFFFu); x[1] = bf16_to_f64(v.x >> 16);
+  x[2] = bf16_to_f64(v.y & 0xFFFFu); x[3] = bf16_to_f64(v.y >> 16);
+  x[4] = bf16_to_f64(v.z & 0xFFFFu); x[5] = bf16_to_f64(v.z >> 16);
+  x[6] = bf16_to_f64(v.w & 0xFFFFu); x[7] = bf16_to_f64(v.w >> 16);
 }
 
 // x / c correctly rounded for a positive integer c, from r = RN(1/c): the
@@ -43,11 +62,13 @@ __device__ __forceinline__ void unpack8(const uint4& v, double (&x)[8]) {
 // corrected quotient RN(q + e r) (P. Markstein, "Computation of elementary
 // functions on the IBM RISC System/6000 processor", IBM J. Res. Develop.
 // 34(1), 1990). fp64 division is slow on this part; one reciprocal then
-// serves the eight channels of a vector. A zero quotient keeps the sign of x.
+// serves the eight channels of a vector. A zero quotient keeps the sign of x;
+// an infinite or NaN quotient is returned as it is (the residual of an
+// infinity would be inf - inf = NaN, where IEEE division gives the infinity).
 // Checked against IEEE division on 2^32 operands shaped like block sums.
 __device__ __forceinline__ double div_by_count(double x, double c, double r) {
   const double q = x * r;
-  if (q == 0.0) return q;
+  if (q == 0.0 || !(fabs(q) <= 1.7976931348623157e308)) return q;
   const double e = fma(-q, c, x);
   return fma(e, r, q);
 }
