@@ -119,8 +119,12 @@ __device__ __forceinline__ int seq_blocks(const ScoreArgs& a, int b) {
 }
 
 // Order-preserving map of fp32 to uint32 (larger float -> larger key); -0 is
-// folded onto +0 first so that equal scores compare equal.
+// folded onto +0 first so that equal scores compare equal, and a NaN score
+// (from non-finite keys) takes the lowest key, below -inf, whatever its sign
+// bit: it is chosen after every number, ties by index, as the Top-k's sort
+// order has it.
 __device__ __forceinline__ uint32_t order_key(float s) {
+  if (s != s) return 0u;
   uint32_t u = __float_as_uint(s + 0.0f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }

@@ -54,6 +54,9 @@ def _rows(rng, nmax):
         (rng.standard_normal(129), 128),
         (rng.standard_normal(nmax), nmax - 1),
         (rng.standard_normal(nmax - 37), 1),
+        # non-finite scores: NaN of either sign ranks below -inf, ties by index
+        (np.concatenate([[np.nan, 1.0, -np.inf, -np.nan, 2.0, np.inf, np.nan],
+                         rng.standard_normal(n(200) - 7)]), n(200) - 3),
     ]
 
 
@@ -71,6 +74,9 @@ def test_threshold_search_paths_match_oracle(K, max_blocks):
     want_vals = []
     for b, (v, _) in enumerate(rows):
         vb = torch.from_numpy(v.astype(np.float32)).to(torch.bfloat16)
+        neg_nan = np.signbit(v) & np.isnan(v)
+        if neg_nan.any():                     # keep the sign bit of a negative NaN
+            vb.view(torch.int16)[torch.from_numpy(neg_nan)] = torch.tensor(-64, dtype=torch.int16)  # 0xFFC0
         summ[b, : len(v), 0, 0] = vb
         want_vals.append(vb.float().numpy().astype(np.float64))
     q = torch.zeros((batch, 1, d), dtype=torch.bfloat16)
@@ -93,7 +99,7 @@ def test_threshold_search_paths_match_oracle(K, max_blocks):
         for b, (v, k) in enumerate(rows):
             N = len(v)
             sc = scores[b, :N].cpu().numpy().astype(np.float64)
-            assert np.array_equal(sc, want_vals[b])
+            assert np.array_equal(sc, want_vals[b], equal_nan=True)
             want = o.topk_blocks(want_vals[b], k)
             got = sel[b, : int(n_sel[b])].cpu().numpy()
             assert np.array_equal(got, want), f"row {b}"

@@ -254,6 +254,15 @@ def test_topk_brute_force_with_ties(seed):
         assert got == want, (scores, k)
 
 
+def test_topk_ranks_nan_below_every_number():
+    # worked by hand: 2 (block 4), 1 (block 1), -inf (block 2), then the NaNs
+    # by index (blocks 0 and 3)
+    s = np.array([np.nan, 1.0, -np.inf, np.nan, 2.0])
+    want = {1: [4], 2: [1, 4], 3: [1, 2, 4], 4: [0, 1, 2, 4], 5: [0, 1, 2, 3, 4]}
+    for k, sel in want.items():
+        assert o.topk_blocks(s, k).tolist() == sel
+
+
 def test_topk_clamps_k():
     s = np.array([3.0, 1.0, 2.0])
     assert o.topk_blocks(s, 7).tolist() == [0, 1, 2]
