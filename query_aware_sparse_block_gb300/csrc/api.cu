@@ -7,6 +7,8 @@
 #include <cstdio>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kvsel_common.cuh"
 #include "kvsel_internal.h"
 
@@ -133,6 +135,16 @@ int check_problem(const kvsel_problem* p) {
   return KVSEL_OK;
 }
 
+// An NVTX range around one entry-point call, named like the entry point, so
+// that a profiler attached to the process (ncu --nvtx, nsys) groups each
+// call's kernels; with no profiler attached, push and pop return at once.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+
 int cuda_status(cudaError_t e, const char* where) {
   if (e == cudaSuccess) return KVSEL_OK;
   set_last_error("%s: %s", where, cudaGetErrorString(e));
@@ -219,6 +231,7 @@ __global__ void wait_selftest_kernel(int* err) {
 extern "C" {
 
 int kvsel_selftest_wait_timeout(kvsel_stream_t stream) {
+  CallRange range("kvsel_selftest_wait_timeout");
   int* ew = device_error_word();
   if (!ew) return fail(KVSEL_ERR_CUDA, "selftest_wait_timeout: no CUDA device");
   wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(ew);
@@ -245,6 +258,7 @@ int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16* kv_pages
                           const int32_t* append_pos, const kvsel_bf16* new_k,
                           const kvsel_bf16* new_v, kvsel_bf16* summaries, double* open_acc,
                           kvsel_stream_t stream) {
+  CallRange range("kvsel_build_summaries");
   int r = check_problem(p);
   if (r) return r;
   if (mode != KVSEL_SUMMARY_FULL && mode != KVSEL_SUMMARY_APPEND)
@@ -318,6 +332,7 @@ int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_bf
                      float tau_rel, int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
                      int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
                      float* scores_out, void* ws, size_t ws_bytes, kvsel_stream_t stream) {
+  CallRange range("kvsel_score_topk");
   int r = check_problem(p);
   if (r) return r;
   if (p->batch == 0) return KVSEL_OK;
@@ -358,6 +373,7 @@ int kvsel_append_score_topk(const kvsel_problem* p, const kvsel_append_in* app,
                             int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
                             float* scores_out, void* ws, size_t ws_bytes,
                             kvsel_stream_t stream) {
+  CallRange range("kvsel_append_score_topk");
   int r = check_problem(p);
   if (r) return r;
   if (!app) return fail(KVSEL_ERR_INVALID_ARG, "append_score_topk: NULL append inputs");
@@ -377,6 +393,7 @@ int kvsel_score_topk_window(const kvsel_problem* p, const kvsel_window* win,
                             int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
                             float* scores_out, void* ws, size_t ws_bytes,
                             kvsel_stream_t stream) {
+  CallRange range("kvsel_score_topk_window");
   int r = check_problem(p);
   if (r) return r;
   if (!win) return fail(KVSEL_ERR_INVALID_ARG, "score_topk_window: NULL window");
@@ -401,6 +418,7 @@ int kvsel_score_topk_window(const kvsel_problem* p, const kvsel_window* win,
 int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, const int32_t* n_sel,
                       int32_t* span_start, int32_t* span_len, int32_t* n_spans,
                       kvsel_stream_t stream) {
+  CallRange range("kvsel_merge_spans");
   int r = check_problem(p);
   if (r) return r;
   if (p->batch == 0) return KVSEL_OK;
@@ -454,6 +472,7 @@ static int check_cache(const char* who, const kvsel_problem* p, const kvsel_bloc
 }
 
 int kvsel_cache_reset(const kvsel_problem* p, const kvsel_block_cache* c, kvsel_stream_t stream) {
+  CallRange range("kvsel_cache_reset");
   int r = check_problem(p);
   if (r) return r;
   r = check_cache("cache_reset", p, c);
@@ -471,6 +490,7 @@ int kvsel_cache_fetch(const kvsel_problem* p, const kvsel_block_cache* c, const 
                       int32_t host_blocks, const int32_t* seq_lens, const int32_t* sel_idx,
                       const int32_t* n_sel, int32_t step, int32_t* n_fetched, int32_t fetch_ctas,
                       void* ws, size_t ws_bytes, kvsel_stream_t stream) {
+  CallRange range("kvsel_cache_fetch");
   int r = check_problem(p);
   if (r) return r;
   r = check_cache("cache_fetch", p, c);
@@ -505,6 +525,7 @@ int kvsel_fetch_spans(const kvsel_problem* p, const kvsel_kv_src* kv, const int3
                       const int32_t* span_start, const int32_t* span_len,
                       const int32_t* n_spans, const uint8_t* dense_flag,
                       kvsel_stream_t stream) {
+  CallRange range("kvsel_fetch_spans");
   int r = check_problem(p);
   if (r) return r;
   if (!kv || kv->kind != KVSEL_KV_HOST)
@@ -530,6 +551,7 @@ int kvsel_sparse_decode(const kvsel_problem* p, const kvsel_bf16* q, const kvsel
                         const int32_t* n_spans, const uint8_t* dense_flag, float softmax_scale,
                         float* out, kvsel_bf16* out_bf16, float* lse, void* ws,
                         size_t ws_bytes, kvsel_stream_t stream) {
+  CallRange range("kvsel_sparse_decode");
   int r = check_problem(p);
   if (r) return r;
   if (!kv) return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: kv is NULL");
