@@ -57,7 +57,44 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
     const int j = v / vec_per_head;
     const int c0 = (v % vec_per_head) * 8;
     const kvsel_bf16* tile = kv_pages + (page * H + j) * 2 * int64_t(B) * d;
+    // the exact sum on the integer pipe (equal to the sequential fp64 sum when
+    // the column's exponents lie within 39 of each other), else the fp64 sum
+    ExactSum es[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) exact_init(es[i]);
+    {
+      int t = 0;
+      for (; t + 8 <= cnt; t += 8) {
+        uint4 r[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) r[u] = ldg_stream(tile + tiled_off(t + u, c0, B));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t w[4] = {r[u].x, r[u].y, r[u].z, r[u].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            exact_add(es[2 * i], w[i] & 0xFFFFu);
+            exact_add(es[2 * i + 1], w[i] >> 16);
+          }
+        }
+      }
+      for (; t < cnt; ++t) {
+        const uint4 r = ldg_stream(tile + tiled_off(t, c0, B));
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          exact_add(es[2 * i], w[i] & 0xFFFFu);
+          exact_add(es[2 * i + 1], w[i] >> 16);
+        }
+      }
+    }
+    bool bad = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bad = bad || es[i].bad;
     double acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = exact_result(es[i]);
+    if (bad) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0.0;
     int t = 0;
@@ -78,6 +115,7 @@ __global__ void __launch_bounds__(kThreads) summaries_full_kernel(
       unpack8(ldg_stream(tile + tiled_off(t, c0, B)), x);
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] += x[i];
+    }
     }
     const int64_t so = ((int64_t(b) * max_blocks + n) * H + j) * d + c0;
     *reinterpret_cast<uint4*>(summaries + so) = mean_to_bf16x8(acc, cnt);

@@ -50,6 +50,61 @@ __device__ __forceinline__ double bf16_to_f64(uint32_t h) {
   return __longlong_as_double(static_cast<long long>(sign | (ex << 52) | man));
 }
 
+// The sum of a block column (at most 64 bf16 values) on the integer pipe.
+// A bf16 value is m * 2^(E - 134) with an integer m < 2^8 and E its biased
+// exponent (E = 1 for subnormals). Let r and E_max be the lowest and highest
+// E among the column's non-zero values. If E_max - r <= 39, every partial sum
+// of the column is an integer multiple of 2^(r - 134) below 2^53 of those
+// units, so each fp64 addition of the sequential sum the summary definition
+// prescribes is exact, and that sum equals the exact sum: accumulated here as
+// an int64 count of units and converted at the end without rounding. A column
+// with a wider spread, an infinity or a NaN is marked `bad`; its caller takes
+// the fp64 sum in token order instead.
+struct ExactSum {
+  long long acc;   // the sum in units of 2^(r - 134)
+  int r, emax;     // lowest and highest biased exponent of the non-zero values
+  bool bad;
+};
+
+__device__ __forceinline__ void exact_init(ExactSum& s) {
+  s.acc = 0;
+  s.r = 255;
+  s.emax = 0;
+  s.bad = false;
+}
+
+__device__ __forceinline__ void exact_add(ExactSum& s, uint32_t h) {
+  if (s.bad) return;
+  const uint32_t e = (h >> 7) & 0xFFu, f = h & 0x7Fu;
+  if (e == 0xFFu) {
+    s.bad = true;
+    return;
+  }
+  if (e == 0u && f == 0u) return;                        // +-0 adds nothing
+  const int ee = e ? int(e) : 1;
+  const int nr = min(s.r, ee), nmax = max(s.emax, ee);
+  if (nmax - nr > 39) {
+    s.bad = true;
+    return;
+  }
+  if (nr < s.r) {
+    if (s.acc != 0) s.acc <<= (s.r - nr);                // at most 39, and |acc| stays < 2^53
+    s.r = nr;
+  }
+  s.emax = nmax;
+  const long long v = static_cast<long long>(e ? (0x80u | f) : f) << (ee - s.r);
+  s.acc += (h & 0x8000u) ? -v : v;
+}
+
+// The exact sum as fp64 (|acc| < 2^53 converts exactly; the power of two
+// 2^(r - 134) is a normal number, so the product is exact). An empty or
+// cancelling column gives +0, as the sequential sum from +0.0 does.
+__device__ __forceinline__ double exact_result(const ExactSum& s) {
+  if (s.acc == 0) return 0.0;
+  const double scale = __longlong_as_double(static_cast<long long>(s.r - 134 + 1023) << 52);
+  return __ll2double_rn(s.acc) * scale;
+}
+
 __device__ __forceinline__ void unpack8(const uint4& v, double (&x)[8]) {
   x[0] = bf16_to_f64(v.x & 0xFFFFu); x[1] = bf16_to_f64(v.x >> 16);
   x[2] = bf16_to_f64(v.y & 0xFFFFu); x[3] = bf16_to_f64(v.y >> 16);

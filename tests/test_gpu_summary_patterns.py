@@ -69,3 +69,52 @@ def test_every_bf16_pattern_through_the_full_build(K, batch):
         assert np.array_equal(np.isnan(a), np.isnan(last))
         fin = ~np.isnan(last)
         assert np.array_equal(a[fin], last[fin]), f"open-block sums differ (seq {s})"
+
+
+def _column_mix(rng, n_blocks, H, B, d):
+    """Keys [n_blocks][H][B][d] whose block columns exercise every path of
+    the summary sum: exponents within a narrow range (the exact integer
+    sum), a range wider than 2^39 (the sequential fp64 sum, which rounds),
+    exact cancellation, and an infinity or a NaN among finite values."""
+    x = rng.standard_normal((n_blocks, H, B, d))
+    kind = rng.integers(0, 5, (n_blocks, H, 1, d))
+    narrow = np.ldexp(x, rng.integers(-15, 16, x.shape))
+    wide = np.ldexp(x, rng.integers(-90, 91, x.shape))
+    cancel = np.concatenate([x[:, :, : B // 2], -x[:, :, : B // 2]], axis=2)
+    special = x.copy()
+    special[:, :, B // 3] = np.where(rng.random((n_blocks, H, d)) < 0.5, np.inf, np.nan)
+    special[:, :, B // 5] = np.where(rng.random((n_blocks, H, d)) < 0.2, -np.inf, special[:, :, B // 5])
+    out = np.select([kind == 0, kind == 1, kind == 2, kind == 3], [x, narrow, wide, cancel], special)
+    return torch.from_numpy(out.astype(np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("H,d,B", [(8, 64, 16), (2, 128, 64)])
+def test_summary_sum_paths_match_the_oracle(K, H, d, B):
+    from query_aware_sparse_block_gb300.runtime import SparseDecoder
+    rng = np.random.default_rng(H * 1000 + B)
+    N, batch = 48, 2
+    kb = _column_mix(rng, batch * N, H, B, d)                  # [pages][H][B][d]
+    dev = "cuda:0"
+    pages = torch.zeros((batch * N, H, 2, d // 64, B, 64), dtype=torch.bfloat16)
+    pages[:, :, 0] = to_tiled(kb)
+    perm = torch.from_numpy(rng.permutation(batch * N).astype(np.int32))
+    pages = pages[perm.argsort()]                             # page perm[i] holds logical block i
+    table = perm.view(batch, N).to(dev)
+    lens = [N * B, N * B - B // 2 - 1]                         # the second ends mid-block
+    dec = SparseDecoder(batch, 4 * H, H, d, B, N, k_max=1, device=dev)
+    summ, acc = dec.new_summaries()
+    dec.build_summaries(pages.to(dev), table, torch.tensor(lens, dtype=torch.int32, device=dev), summ, acc)
+    torch.cuda.synchronize()
+    assert K.kvsel_get_error() == 0
+    for s in range(batch):
+        T = lens[s]
+        kseq = bits(kb[s * N:(s + 1) * N].permute(0, 2, 1, 3).reshape(N * B, H, d))[:T]
+        want, _, last = o.block_summaries(kseq, T, B)
+        got = bits(summ[s])
+        nan_w, nan_g = _is_nan(want), _is_nan(got)
+        assert np.array_equal(nan_w, nan_g), f"NaN positions differ (seq {s})"
+        assert np.array_equal(np.where(nan_w, 0, want), np.where(nan_g, 0, got)), f"summaries differ (seq {s})"
+        a = acc[s].cpu().numpy()
+        assert np.array_equal(np.isnan(a), np.isnan(last))
+        fin = ~np.isnan(last)
+        assert np.array_equal(a[fin], last[fin]), f"open-block sums differ (seq {s})"
