@@ -21,6 +21,7 @@ bounded sample (one layer, a few sequences) of the same workload.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import math
@@ -871,28 +872,36 @@ def run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs, uncached_
     q = x["q"].float()
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     rows, host_us = [], []
-    for step in range(steps):
-        if step:
-            q = rho * q + math.sqrt(1 - rho * rho) * torch.randn(q.shape, generator=g, device=device)
-        qb = q.to(torch.bfloat16)
-        torch.cuda.synchronize()
-        # a bounded device-side delay (about 1 ms) while the host enqueues the
-        # whole step, so that the events time the GPU and not the host calls
-        torch.cuda._sleep(2_000_000)
-        ev[0].record()
-        dec.select(qb, summ, x["seq_lens"], gamma=w.gamma)
-        ev[1].record()
-        h0 = time.perf_counter()
-        cache.fetch(host, N, x["seq_lens"], dec.sel_idx, dec.n_sel)
-        host_us.append((time.perf_counter() - h0) * 1e6)
-        ev[2].record()
-        dec.attend(qb, cache.kv, x["seq_lens"], use_dense_flag=False)
-        ev[3].record()
-        torch.cuda.synchronize()
-        if int(dec.dense_flag.sum()):
-            raise RuntimeError("a sequence went dense at the keep floor")
-        fetched = int(cache.n_fetched.sum())
-        rows.append((fetched, ev[1].elapsed_time(ev[2]) * 1e3, ev[0].elapsed_time(ev[3]) * 1e3))
+    # no collector pause may fall between two of a step's calls (the events
+    # would then time an idle GPU)
+    gc_was_on = gc.isenabled()
+    gc.disable()
+    try:
+        for step in range(steps):
+            if step:
+                q = rho * q + math.sqrt(1 - rho * rho) * torch.randn(q.shape, generator=g, device=device)
+            qb = q.to(torch.bfloat16)
+            torch.cuda.synchronize()
+            # a bounded device-side delay (about 4 ms) while the host enqueues the
+            # whole step, so that the events time the GPU and not the host calls
+            torch.cuda._sleep(8_000_000)
+            ev[0].record()
+            dec.select(qb, summ, x["seq_lens"], gamma=w.gamma)
+            ev[1].record()
+            h0 = time.perf_counter()
+            cache.fetch(host, N, x["seq_lens"], dec.sel_idx, dec.n_sel)
+            host_us.append((time.perf_counter() - h0) * 1e6)
+            ev[2].record()
+            dec.attend(qb, cache.kv, x["seq_lens"], use_dense_flag=False)
+            ev[3].record()
+            torch.cuda.synchronize()
+            if int(dec.dense_flag.sum()):
+                raise RuntimeError("a sequence went dense at the keep floor")
+            fetched = int(cache.n_fetched.sum())
+            rows.append((fetched, ev[1].elapsed_time(ev[2]) * 1e3, ev[0].elapsed_time(ev[3]) * 1e3))
+    finally:
+        if gc_was_on:
+            gc.enable()
     err = K.kvsel_get_error()
     if err:
         raise RuntimeError(f"device error {err} in the block-cache measurement")
@@ -908,6 +917,7 @@ def run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs, uncached_
             "hit_rate": 1.0 - blocks / (w.batch * k), "link_bytes_per_step": link,
             "fetch_us": fetch_us, "fetch_gbs": link / (fetch_us / 1e6) / 1e9,
             "frac_of_h2d_copy": link / (fetch_us / 1e6) / 1e9 / h2d_gbs,
+            "fetch_gbs_median_step": statistics.median(r[0] * page_bytes / r[1] / 1e3 for r in warm),
             "select_fetch_attend_us": step_us, "uncached_fetch_plus_attend_us": uncached_us,
             "fetch_call_host_us": statistics.median(host_us),
             "per_step": [[r[0], round(r[1], 1)] for r in rows]}

@@ -406,7 +406,7 @@ KVSEL_API int kvsel_cache_reset(const kvsel_problem* p, const kvsel_block_cache*
  * step: >= 0 and different from the step of the previous call on this cache
  * (a step counter). slots >= k_max guarantees a free slot for every miss.
  * ws: kvsel_workspace_size(p, KVSEL_WS_CACHE_FETCH) bytes (job lists; no
- * initial contents required). fetch_ctas: CTAs of the copy kernel (0 = one
+ * initial contents required). fetch_ctas: CTAs of the copy kernel (0 = eight
  * per SM). Errors: INVALID_ARG (NULL or misaligned pointer, slots outside
  * [k_max, 4096], step < 0, host_kv not device-mapped pinned memory),
  * WORKSPACE, UNSUPPORTED, CUDA; device BOUNDS for a selection that is not

@@ -241,7 +241,10 @@ cudaError_t launch_cache_fetch(const kvsel_problem& p, const kvsel_block_cache& 
   count_launch();
   if (e != cudaSuccess) return e;
   const int64_t block_vec = int64_t(2) * p.n_kvheads * p.block_size * p.head_dim * 2 / 16;
-  const int ctas = fetch_ctas > 0 ? fetch_ctas : sm_count();
+  // default: eight CTAs per SM, so that a sequence with many misses spreads them over
+  // many CTAs (64 sequences of 64 KiB blocks: 190-200 GB/s with one CTA per SM,
+  // 201-202 GB/s with four to sixteen per SM)
+  const int ctas = fetch_ctas > 0 ? fetch_ctas : 8 * sm_count();
   int per_seq = std::max(1, (ctas + p.batch - 1) / p.batch);
   per_seq = std::min(per_seq, p.k_max + 1);
   cache_copy_kernel<<<dim3(per_seq, p.batch), kCopyThreads, 0, s>>>(
