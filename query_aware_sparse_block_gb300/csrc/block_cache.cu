@@ -244,9 +244,9 @@ cudaError_t launch_cache_fetch(const kvsel_problem& p, const kvsel_block_cache& 
   // default: eight CTAs per SM, so that a sequence with many misses spreads them over
   // many CTAs (64 sequences of 64 KiB blocks: 190-200 GB/s with one CTA per SM,
   // 201-202 GB/s with four to sixteen per SM)
-  const int ctas = fetch_ctas > 0 ? fetch_ctas : 8 * sm_count();
-  int per_seq = std::max(1, (ctas + p.batch - 1) / p.batch);
-  per_seq = std::min(per_seq, p.k_max + 1);
+  const int64_t ctas = fetch_ctas > 0 ? fetch_ctas : 8 * sm_count();
+  const int per_seq = int(std::min<int64_t>(std::max<int64_t>(1, (ctas + p.batch - 1) / p.batch),
+                                            int64_t(p.k_max) + 1));
   cache_copy_kernel<<<dim3(per_seq, p.batch), kCopyThreads, 0, s>>>(
       host_kv, c.pool, a.jobs, a.n_jobs, host_blocks, p.k_max, block_vec, err);
   count_launch();

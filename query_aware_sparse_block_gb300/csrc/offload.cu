@@ -101,9 +101,9 @@ cudaError_t launch_fetch_spans(const kvsel_problem& p, const kvsel_kv_src& kv,
                                const uint8_t* dense_flag, int* err, cudaStream_t s) {
   if (p.batch == 0) return cudaSuccess;
   const int64_t block_vec = int64_t(2) * p.n_kvheads * p.block_size * p.head_dim * 2 / 16;
-  int ctas = kv.fetch_ctas > 0 ? kv.fetch_ctas : sm_count();
-  int per_seq = std::max(1, (ctas + p.batch - 1) / p.batch);
-  per_seq = std::min(per_seq, std::max(1, kv.staging_slots));
+  const int64_t ctas = kv.fetch_ctas > 0 ? kv.fetch_ctas : sm_count();
+  const int per_seq = int(std::min<int64_t>(std::max<int64_t>(1, (ctas + p.batch - 1) / p.batch),
+                                            std::max(1, kv.staging_slots)));
   dim3 grid(per_seq, p.batch);
   const size_t smem = (size_t(p.k_max) + 1) * 4;
   if (smem > 48 * 1024) {
