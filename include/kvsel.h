@@ -143,10 +143,15 @@ KVSEL_API int kvsel_build_summaries(const kvsel_problem* p, int mode, kvsel_bf16
  * kvsel_score_topk -- query-aware block score, Top-k and span merge
  * ("SparPR KV cache recovery on a consumer GPU", paragraphs "Query-Aware
  * key-block selection" and "On-demand local recomputation with cost-aware
- * fallback"). Enqueues two kernels on `stream` (scores, then Top-k). The
- * score kernel is launched with programmatic stream serialization: it may
- * become resident while the kernel before it still runs, but reads no input
- * before that kernel has completed, so stream order is kept.
+ * fallback"). Enqueues on `stream` either one kernel -- one thread-block
+ * cluster per sequence scores the sequence's blocks and its leader CTA ranks
+ * them, when every sequence's cluster fits on the device at once and
+ * max_blocks <= 4096 -- or two (a score grid, then one Top-k CTA per
+ * sequence); kvsel_score_path_for() tells which. Both give the same results
+ * bit for bit. The first kernel is launched with programmatic stream
+ * serialization: it may become resident while the kernel before it still
+ * runs, but reads no input before that kernel has completed, so stream order
+ * is kept.
  *
  * score[b][n] = sum over query heads h of <q[b][h], summaries[b][n][kv(h)]>,
  * kv(h) = h / G, accumulated in fp32 (q is first folded over each GQA group).
@@ -171,6 +176,33 @@ KVSEL_API int kvsel_score_topk(const kvsel_problem* p, const kvsel_bf16* q, cons
                      int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
                      float* scores_out, void* ws, size_t ws_bytes, kvsel_stream_t stream);
 
+/* Which form the score + Top-k calls take (kvsel_set_score_path). */
+enum kvsel_score_path {
+  KVSEL_SCORE_PATH_AUTO = 0,     /* one launch of clusters where the problem allows, else two grids */
+  KVSEL_SCORE_PATH_TWO_GRID = 1, /* always the score grid + Top-k grid */
+  KVSEL_SCORE_PATH_CLUSTER = 2   /* always the cluster launch; other problems fail with UNSUPPORTED */
+};
+
+/*
+ * kvsel_set_score_path -- process-wide choice of the form every later
+ * kvsel_score_topk, kvsel_append_score_topk, kvsel_score_topk_window and
+ * kvsel_score_topk_noalloc call takes (default AUTO). The forms compute the
+ * same results bit for bit; the choice exists for measurement and tests.
+ * Returns the previous value, or -1 (and changes nothing) for an unknown one.
+ * Not synchronised with calls running in other host threads.
+ */
+KVSEL_API int kvsel_set_score_path(int path);
+
+/*
+ * kvsel_score_path_for -- the form (KVSEL_SCORE_PATH_TWO_GRID or
+ * KVSEL_SCORE_PATH_CLUSTER) a score + Top-k call on problem p takes on the
+ * current device under the current setting, with (with_append != 0) or
+ * without a folded append; *cluster_ctas (nullable) receives the CTAs per
+ * sequence of the cluster form (0 for the two-grid form). Returns a negative
+ * KVSEL_ERR_* code on an invalid problem.
+ */
+KVSEL_API int kvsel_score_path_for(const kvsel_problem* p, int with_append, int32_t* cluster_ctas);
+
 /* The inputs of the APPEND mode of kvsel_build_summaries, for the fused call
  * below. Pointers are device pointers with the meaning, layout and alignment
  * given there; new_k and new_v are nullable (new_v needs new_k). */
@@ -187,7 +219,7 @@ typedef struct kvsel_append_in {
 
 /*
  * kvsel_append_score_topk -- kvsel_build_summaries(APPEND) followed by
- * kvsel_score_topk on the updated table, in the two kernels of
+ * kvsel_score_topk on the updated table, in the kernel(s) of
  * kvsel_score_topk (the decode step of "SparPR KV cache recovery on a
  * consumer GPU", paragraph "Query-Aware key-block selection": the new token's
  * key updates its block's summary before the query scores the blocks).

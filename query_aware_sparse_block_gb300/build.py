@@ -21,8 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkvsel.so")
 
-SOURCES = ["api.cu", "summaries.cu", "score_topk.cu", "sparse_decode.cu", "offload.cu", "noalloc.cu",
-           "block_cache.cu"]
+SOURCES = ["api.cu", "summaries.cu", "score_topk.cu", "score_cluster.cu", "sparse_decode.cu", "offload.cu",
+           "noalloc.cu", "block_cache.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

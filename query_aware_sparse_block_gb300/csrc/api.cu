@@ -319,6 +319,10 @@ static int score_topk_impl(const char* who, const kvsel_problem* p, const kvsel_
     std::snprintf(msg, sizeof msg, "%s: no CUDA device", who);
     return fail(KVSEL_ERR_CUDA, msg);
   }
+  if (score_path() == KVSEL_SCORE_PATH_CLUSTER && score_cluster_size(*p, app != nullptr) == 0) {
+    std::snprintf(msg, sizeof msg, "%s: the cluster form was requested but does not fit this problem", who);
+    return fail(KVSEL_ERR_UNSUPPORTED, msg);
+  }
   std::snprintf(msg, sizeof msg, "%s launch", who);
   return cuda_status(launch_score_topk(*p, q, summaries, seq_lens, k_per_seq, gamma, tau_rel,
                                        sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
@@ -413,6 +417,23 @@ int kvsel_score_topk_window(const kvsel_problem* p, const kvsel_window* win,
   return score_topk_impl("score_topk_window", p, q, summaries, seq_lens, k_per_seq, gamma,
                          tau_rel, sel_idx, n_sel, span_start, span_len, n_spans, dense_flag,
                          scores_out, ws, ws_bytes, app, win->n_sink, win->n_recent, stream);
+}
+
+int kvsel_set_score_path(int path) {
+  if (path != KVSEL_SCORE_PATH_AUTO && path != KVSEL_SCORE_PATH_TWO_GRID &&
+      path != KVSEL_SCORE_PATH_CLUSTER)
+    return -1;
+  const int prev = score_path();
+  set_score_path(path);
+  return prev;
+}
+
+int kvsel_score_path_for(const kvsel_problem* p, int with_append, int32_t* cluster_ctas) {
+  int r = check_problem(p);
+  if (r) return -r;
+  const int C = score_path() == KVSEL_SCORE_PATH_TWO_GRID ? 0 : score_cluster_size(*p, with_append != 0);
+  if (cluster_ctas) *cluster_ctas = C;
+  return C > 0 ? KVSEL_SCORE_PATH_CLUSTER : KVSEL_SCORE_PATH_TWO_GRID;
 }
 
 int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, const int32_t* n_sel,

@@ -40,6 +40,23 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
                               int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
                               float* scores_out, void* ws, const kvsel_append_in* app,
                               int n_sink, int n_recent, int* err, cudaStream_t s);
+// The one-launch form of launch_score_topk (score_cluster.cu): one
+// thread-block cluster per sequence. *launched = false (and nothing enqueued)
+// when the problem is outside that form; launch_score_topk then uses its
+// two grids.
+cudaError_t launch_score_topk_cluster(const kvsel_problem& p, const kvsel_bf16* q,
+                                      const kvsel_bf16* summaries, const int32_t* seq_lens,
+                                      const int32_t* k_per_seq, float gamma, float tau_rel,
+                                      int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                                      int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                                      float* scores_out, const kvsel_append_in* app, int n_sink,
+                                      int n_recent, int* err, cudaStream_t s, bool* launched);
+// CTAs per cluster the one-launch form takes for p on the current device (0:
+// outside it).
+int score_cluster_size(const kvsel_problem& p, bool app);
+// Process-wide choice between the forms (KVSEL_SCORE_PATH_*).
+void set_score_path(int path);
+int score_path();
 cudaError_t launch_merge_spans(const kvsel_problem& p, const int32_t* sel_idx,
                                const int32_t* n_sel, int32_t* span_start, int32_t* span_len,
                                int32_t* n_spans, int* err, cudaStream_t s);

@@ -33,6 +33,9 @@ KVSEL_KV_HOST_DIRECT = 3
 KVSEL_WS_SCORE_TOPK = 0
 KVSEL_WS_SPARSE_DECODE = 1
 KVSEL_WS_CACHE_FETCH = 2
+KVSEL_SCORE_PATH_AUTO = 0
+KVSEL_SCORE_PATH_TWO_GRID = 1
+KVSEL_SCORE_PATH_CLUSTER = 2
 
 _STATUS = {1: "INVALID_ARG", 2: "CUDA", 3: "BOUNDS", 4: "TIMEOUT", 5: "UNSUPPORTED", 6: "WORKSPACE"}
 
@@ -107,6 +110,8 @@ _SIGS = {
     "kvsel_score_topk_noalloc": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, ctypes.c_float,
                                       ctypes.c_float, _P, _P, _P, _P, _P, _P, _P, _P]),
     "kvsel_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "kvsel_set_score_path": (_I, [_I]),
+    "kvsel_score_path_for": (_I, [ctypes.POINTER(kvsel_problem), _I, ctypes.POINTER(ctypes.c_int32)]),
     "kvsel_merge_spans": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, _P, _P]),
     "kvsel_sparse_decode": (_I, [ctypes.POINTER(kvsel_problem), _P, ctypes.POINTER(kvsel_kv_src), _P,
                                  _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
@@ -202,6 +207,23 @@ def kvsel_kv_bytes_per_token(layers, kv_heads, head_dim, elem_bytes) -> int:
 
 def kvsel_workspace_size(p: kvsel_problem, which: int) -> int:
     return int(lib().kvsel_workspace_size(ctypes.byref(p), which))
+
+
+def kvsel_set_score_path(path: int) -> int:
+    """Process-wide form of the score + Top-k calls; returns the previous one."""
+    prev = lib().kvsel_set_score_path(int(path))
+    if prev < 0:
+        raise KvselError(KVSEL_ERR_INVALID_ARG, "kvsel_set_score_path", f"unknown path {path}")
+    return prev
+
+
+def kvsel_score_path_for(p: kvsel_problem, with_append: bool = False):
+    """(form, CTAs per cluster) a score + Top-k call on p would take."""
+    ctas = ctypes.c_int32(0)
+    r = lib().kvsel_score_path_for(ctypes.byref(p), int(bool(with_append)), ctypes.byref(ctas))
+    if r < 0:
+        _check(-r, "kvsel_score_path_for")
+    return r, int(ctas.value)
 
 
 def kvsel_budget(block_size, kv_heads, head_dim, elem_bytes, hidden, n_blocks, h2d_bytes_per_s,

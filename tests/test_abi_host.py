@@ -198,3 +198,24 @@ def test_header_compiles_as_c_and_the_library_links_from_c(K, tmp_path):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.strip().endswith("all ok")
+
+
+def test_score_path_setting_is_validated(K):
+    """kvsel_set_score_path accepts the three forms and returns the previous
+    one; an unknown value changes nothing. kvsel_score_path_for names one of
+    the two forms (without a GPU: the two-grid form) and rejects a bad shape."""
+    L = K.lib()
+    assert L.kvsel_set_score_path(7) == -1
+    assert K.kvsel_set_score_path(K.KVSEL_SCORE_PATH_TWO_GRID) == K.KVSEL_SCORE_PATH_AUTO
+    assert K.kvsel_set_score_path(K.KVSEL_SCORE_PATH_CLUSTER) == K.KVSEL_SCORE_PATH_TWO_GRID
+    assert K.kvsel_set_score_path(K.KVSEL_SCORE_PATH_AUTO) == K.KVSEL_SCORE_PATH_CLUSTER
+    p = K.problem(16, 32, 8, 128, 32, 1024, 128)
+    form, ctas = K.kvsel_score_path_for(p)
+    assert form in (K.KVSEL_SCORE_PATH_TWO_GRID, K.KVSEL_SCORE_PATH_CLUSTER)
+    assert (ctas == 0) == (form == K.KVSEL_SCORE_PATH_TWO_GRID)
+    K.kvsel_set_score_path(K.KVSEL_SCORE_PATH_TWO_GRID)
+    assert K.kvsel_score_path_for(p) == (K.KVSEL_SCORE_PATH_TWO_GRID, 0)
+    K.kvsel_set_score_path(K.KVSEL_SCORE_PATH_AUTO)
+    bad = K.problem(16, 32, 8, 96, 32, 1024, 128)       # head_dim 96 is not supported
+    with pytest.raises(K.KvselError):
+        K.kvsel_score_path_for(bad)
