@@ -493,6 +493,9 @@ def run_gpu(args):
         configs = run_configs(device)
         configs.append(run_summary_build(device))
 
+    form, ctas = K.kvsel_score_path_for(wb.dec.p, True)
+    score_form = {"form": "cluster" if form == K.KVSEL_SCORE_PATH_CLUSTER else "two_grid",
+                  "cluster_ctas": ctas}
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_rate(world, layers, args.steps, elapsed_ms)
     peak, peak_kind = peaks()
@@ -512,7 +515,8 @@ def run_gpu(args):
                    "n_kvheads": w.n_kvheads, "head_dim": w.head_dim, "seq_len": w.seq_len,
                    "block_size": w.block_size, "keep": w.keep[0], "k": wb.k, "layers": layers,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (distinct buffers per layer, no flush)"},
+                   "l2": "inputs larger than L2 (distinct buffers per layer, no flush)",
+                   "score_form": score_form},
         "roofline": {"kernel": "sparse_decode", "bound": "hbm", "achieved": dec_gbs, "peak": peak,
                      "unit": "GB/s", "frac": dec_gbs / peak, "peak_kind": peak_kind,
                      "frac_of_nominal": dec_gbs / NOMINAL_HBM_GBS,

@@ -329,7 +329,10 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_cluster_kernel(ScoreAr
           }
         }
       }
-      // refill this stage with this warp's chunk S ahead
+      // Refill this stage with this warp's chunk S ahead (lane 0). Every value
+      // the lanes read from the stage has been used by the scores above, so
+      // those reads are complete before the warp barrier and the copy cannot
+      // overwrite bytes still to be read.
       __syncwarp();
       const int c2 = c + S;
       if (c2 < nch && lane == 0) {
@@ -337,7 +340,6 @@ __global__ void __launch_bounds__(kThreads, 1) score_topk_cluster_kernel(ScoreAr
         const int n2 = min(min(CHB, n_hi - cb2), N - cb2);
         if (n2 > 0) {
           const uint32_t bytes = uint32_t(n2) * block_bytes;
-          fence_proxy_async();
           mbar_arrive_expect_tx(&full[s], bytes);
           bulk_load_hint(stage + size_t(s) * SB, a.summaries + (row0 + cb2) * NV * 8, bytes, &full[s], pol);
         }
