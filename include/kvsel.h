@@ -23,8 +23,13 @@
  *    error word and carries on. kvsel_get_error() reads and clears it.
  *  - Device entry points are asynchronous on the caller's stream; the caller
  *    owns every buffer. Scratch comes from a caller workspace whose size
- *    kvsel_workspace_size() returns; a workspace must be zero-filled before
- *    its first use and each call leaves it zero-filled again.
+ *    kvsel_workspace_size() returns. No workspace needs particular initial
+ *    contents: every byte a call reads from its workspace, that call wrote
+ *    first. Calls that share a workspace must not overlap on the GPU.
+ *  - The library looks up the device addresses of its own device variables
+ *    (the error word, the static scratch array) once per device and keeps
+ *    them for the life of the process: do not keep using it on a device
+ *    after cudaDeviceReset() on that device.
  *  - bf16 tensors are passed as kvsel_bf16 (the 16-bit pattern). Device
  *    pointers must be 16-byte aligned.
  *  - Supported shapes: head_dim in {64, 128}; block_size in {16, 32, 64};
@@ -309,7 +314,8 @@ KVSEL_API int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, 
  * bytes (4 MiB) that every GPU which loads the library holds until the
  * process exits. A problem whose kvsel_workspace_size(p, KVSEL_WS_SCORE_TOPK)
  * exceeds it (roughly batch * max_blocks > 1M) is rejected with
- * KVSEL_ERR_WORKSPACE and nothing is enqueued. The first call on a device
+ * KVSEL_ERR_WORKSPACE and nothing is enqueued; the limit applies whether or
+ * not scores_out is given. The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture. Nothing in the
  * array needs to start at zero, so no call clears it; no call allocates.
@@ -514,6 +520,21 @@ KVSEL_API int kvsel_get_error(kvsel_stream_t stream);
  * kvsel_get_error() returns KVSEL_ERR_TIMEOUT (and clears it).
  */
 KVSEL_API int kvsel_selftest_wait_timeout(kvsel_stream_t stream);
+
+/*
+ * kvsel_selftest_divide -- applies, on the device, the division with which
+ * the summary kernels form a block mean (an fp64 key sum over a token count:
+ * one correctly rounded reciprocal, the product, its exact residual and one
+ * correction step, in place of an fp64 division per channel) to n given
+ * pairs: out[i] = x[i] / count[i] as those kernels compute it, before the
+ * rounding to bf16. The pages describe no such call; it lets a test check
+ * that division against IEEE division (the summaries are bit-exact only if
+ * it is correctly rounded). x, out: device fp64 [n], 8-byte aligned; count:
+ * device int32 [n], each >= 1. Enqueued on `stream`. Errors: INVALID_ARG for
+ * n < 0, NULL or misaligned pointers; CUDA.
+ */
+KVSEL_API int kvsel_selftest_divide(const double* x, const int32_t* count, double* out, int64_t n,
+                                    kvsel_stream_t stream);
 
 /* Kernel launches made by this library since load (host-side counter). */
 KVSEL_API uint64_t kvsel_launch_count(void);

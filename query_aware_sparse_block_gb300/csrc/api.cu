@@ -239,6 +239,18 @@ int kvsel_selftest_wait_timeout(kvsel_stream_t stream) {
   return cuda_status(cudaGetLastError(), "selftest_wait_timeout launch");
 }
 
+int kvsel_selftest_divide(const double* x, const int32_t* count, double* out, int64_t n,
+                          kvsel_stream_t stream) {
+  CallRange range("kvsel_selftest_divide");
+  if (n < 0) return fail(KVSEL_ERR_INVALID_ARG, "selftest_divide: n must be >= 0");
+  if (n == 0) return KVSEL_OK;
+  if (!x || !count || !out) return fail(KVSEL_ERR_INVALID_ARG, "selftest_divide: NULL pointer");
+  if ((reinterpret_cast<uintptr_t>(x) & 7u) || (reinterpret_cast<uintptr_t>(out) & 7u) || !aligned4(count))
+    return fail(KVSEL_ERR_INVALID_ARG, "selftest_divide: misaligned pointer");
+  return cuda_status(launch_selftest_divide(x, count, out, n, reinterpret_cast<cudaStream_t>(stream)),
+                     "selftest_divide launch");
+}
+
 int kvsel_get_error(kvsel_stream_t stream) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int r = cuda_status(cudaStreamSynchronize(s), "kvsel_get_error: stream sync");

@@ -3,7 +3,6 @@
 // for sm_103a, and bounded waits.
 #pragma once
 
-#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -107,17 +106,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
-// --------------------------------------------------------------- TMA copy ---
-
-// 2-D tiled tensor load global -> shared, completion counted on `bar`.
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int32_t c0,
-                                            int32_t c1, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-      : "memory");
-}
+// ------------------------------------------------------- bulk (TMA) copy ---
 
 // 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16),
 // completion counted on `bar`.
@@ -146,20 +135,6 @@ __device__ __forceinline__ void bulk_load_hint(void* smem_dst, const void* src, 
       " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(smem_dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
-}
-
-// 4-D tiled tensor load global -> shared, completion counted on `bar`.
-__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int32_t c0,
-                                            int32_t c1, int32_t c2, int32_t c3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // --------------------------------------------------------------- ldmatrix ---

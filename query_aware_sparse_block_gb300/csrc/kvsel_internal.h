@@ -29,6 +29,11 @@ cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16*
                                    kvsel_bf16* summaries, double* open_acc, int* err,
                                    cudaStream_t s);
 
+// The block-mean division of the summary kernels on given (sum, count) pairs
+// (summaries.cu), for kvsel_selftest_divide.
+cudaError_t launch_selftest_divide(const double* x, const int32_t* cnt, double* out, int64_t n,
+                                   cudaStream_t s);
+
 // ---- score + Top-k + spans (score_topk.cu); app != nullptr folds the
 // APPEND summary update into the score grid; the first n_sink and the last
 // n_recent blocks of every sequence are selected whatever their score ----

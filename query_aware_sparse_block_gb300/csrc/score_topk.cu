@@ -352,7 +352,8 @@ __global__ void merge_spans_kernel(const int32_t* __restrict__ sel_idx, const in
 }  // namespace
 
 size_t score_topk_ws_bytes(const kvsel_problem& p) {
-  // a reserved (zero-filled) word per sequence, then the fp32 score rows
+  // a reserved word per sequence (never read or written), then the fp32
+  // score rows; nothing in it needs initial contents
   const size_t reserved = (size_t(p.batch) * 4 + 255) / 256 * 256;
   const size_t scores = size_t(p.batch) * p.max_blocks * 4;
   return reserved + scores;

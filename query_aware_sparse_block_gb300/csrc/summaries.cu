@@ -181,6 +181,17 @@ __global__ void __launch_bounds__(kThreads) summaries_append_kernel(
   }
 }
 
+// The division of a block mean, applied to given (sum, count) pairs: the
+// same reciprocal and correction step as mean_to_bf16x8, without the final
+// rounding to bf16.
+__global__ void selftest_divide_kernel(const double* __restrict__ x, const int32_t* __restrict__ cnt,
+                                       double* __restrict__ out, int64_t n) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += int64_t(gridDim.x) * blockDim.x) {
+    const double c = static_cast<double>(cnt[i]);
+    out[i] = div_by_count(x[i], c, 1.0 / c);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16* kv_pages,
@@ -202,6 +213,15 @@ cudaError_t launch_build_summaries(const kvsel_problem& p, int mode, kvsel_bf16*
         kv_pages, n_pages, block_table, append_pos, new_k, new_v, summaries, open_acc, p.n_kvheads,
         p.head_dim, p.block_size, p.max_blocks, err);
   }
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_divide(const double* x, const int32_t* cnt, double* out, int64_t n,
+                                   cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>(int64_t(sm_count()) * 8, (n + 255) / 256);
+  selftest_divide_kernel<<<unsigned(blocks), 256, 0, s>>>(x, cnt, out, n);
   count_launch();
   return cudaGetLastError();
 }

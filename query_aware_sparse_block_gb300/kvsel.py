@@ -127,6 +127,7 @@ _SIGS = {
     "kvsel_kv_bytes_per_token": (ctypes.c_int64, [ctypes.c_int32] * 4),
     "kvsel_get_error": (_I, [_P]),
     "kvsel_selftest_wait_timeout": (_I, [_P]),
+    "kvsel_selftest_divide": (_I, [_P, _P, _P, ctypes.c_int64, _P]),
     "kvsel_launch_count": (ctypes.c_uint64, []),
     "kvsel_last_error": (ctypes.c_char_p, []),
     "kvsel_version": (ctypes.c_char_p, []),
@@ -235,6 +236,16 @@ def kvsel_budget(block_size, kv_heads, head_dim, elem_bytes, hidden, n_blocks, h
     o = kvsel_budget_out()
     _check(lib().kvsel_budget(ctypes.byref(i), ctypes.byref(o)), "kvsel_budget")
     return o
+
+
+def kvsel_selftest_divide(x, count, out, stream=None):
+    """out = x / count as the summary kernels divide a block sum by its
+    token count (fp64 x and out, int32 count, device tensors)."""
+    _expect(x, torch.float64, "x")
+    _expect(count, torch.int32, "count")
+    _expect(out, torch.float64, "out")
+    _check(lib().kvsel_selftest_divide(_ptr(x), _ptr(count), _ptr(out), x.numel(), _stream(stream)),
+           "kvsel_selftest_divide")
 
 
 def kvsel_selftest_wait_timeout(stream=None):

@@ -35,7 +35,7 @@ class SparseDecoder:
         if ws1 == 0 or ws2 == 0:
             raise K.KvselError(K.KVSEL_ERR_UNSUPPORTED, "SparseDecoder",
                                K.lib().kvsel_last_error().decode())
-        # workspaces start zero-filled; the kernels leave them zero-filled
+        # no workspace needs initial contents; zero-filled only for tidiness
         self.ws_score = torch.zeros((ws1,), dtype=torch.uint8, device=self.device)
         self.ws_decode = torch.zeros((ws2,), dtype=torch.uint8, device=self.device)
         self.out = torch.zeros((b, n_qheads, head_dim), dtype=torch.float32, device=self.device)

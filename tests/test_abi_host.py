@@ -219,3 +219,13 @@ def test_score_path_setting_is_validated(K):
     bad = K.problem(16, 32, 8, 96, 32, 1024, 128)       # head_dim 96 is not supported
     with pytest.raises(K.KvselError):
         K.kvsel_score_path_for(bad)
+
+
+def test_selftest_divide_validates_arguments(K):
+    """kvsel_selftest_divide rejects a negative count of pairs and NULL
+    pointers before anything is enqueued; n = 0 is a no-op."""
+    import ctypes
+    L = K.lib()
+    assert L.kvsel_selftest_divide(None, None, None, ctypes.c_int64(-1), None) == K.KVSEL_ERR_INVALID_ARG
+    assert L.kvsel_selftest_divide(None, None, None, ctypes.c_int64(0), None) == K.KVSEL_OK
+    assert L.kvsel_selftest_divide(None, None, None, ctypes.c_int64(4), None) == K.KVSEL_ERR_INVALID_ARG

@@ -248,13 +248,16 @@ def test_c2_minicpm_gqa16(K):
 
 
 def test_c3_qwen3_4b_batch16(K):
-    _full_layer(K, C3, C3.k_for(C3.keep[0]), sample=[0, 5, 15])
+    _full_layer(K, C3, C3.k_for(C3.keep[0]))
 
 
 def test_c4_offload_tier_fetch_then_decode(K):
-    """Full C4 shape: K/V in pinned host memory, summaries on the GPU, the
-    selected spans fetched over the host link, attention over the staging
-    buffer; sampled sequences against the oracle, plus the dense fallback."""
+    """Full C4 shape at the 5 % Minimum Keep Floor: K/V in pinned host memory,
+    summaries on the GPU, the selected spans fetched over the host link,
+    attention over the staging buffer; every sequence against the oracle
+    (selection under the tie rule, no sequence dense at this keep ratio, and
+    attention). The dense fallback of the host tier is checked by
+    test_offload_staged_dense_fallback_mixed."""
     w = C4
     k = w.k_for(w.keep_floor)
     x = generate_layer(w, 0, device="cuda:0", perm=False)
@@ -275,7 +278,7 @@ def test_c4_offload_tier_fetch_then_decode(K):
     kv = KK.kv_host(host, N, staging, slots)
     dec.attend(x["q"], kv, x["seq_lens"])
     torch.cuda.synchronize()
-    for b in (0, 31, 63):
+    for b in range(w.batch):
         qb = bits(x["q"][b])
         kb = bits(natural_blocks(host[b, :, :, 0]).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
         vb = bits(natural_blocks(host[b, :, :, 1]).reshape(N * w.block_size, w.n_kvheads, w.head_dim))
@@ -291,3 +294,45 @@ def test_c4_offload_tier_fetch_then_decode(K):
     b = 7
     gsel = dec.sel_idx[b, : int(dec.n_sel[b])].cpu()
     assert torch.equal(staging[b, :5].cpu(), host[b, gsel[:5].long()])
+
+
+def test_offload_staged_dense_fallback_mixed(K):
+    """The host tier through KVSEL_KV_HOST (the selected spans, or every block
+    of a dense sequence, gathered into staging, then attended) with the gamma
+    rule deciding per sequence ("SparPR KV cache recovery on a consumer GPU",
+    paragraph "On-demand local recomputation with cost-aware fallback": once
+    the sparse path is no longer clearly cheaper, recover everything). The
+    copy/recompute model gives r = 1 for the C4 shape with GB300-class link and
+    compute rates, so k = N and every sequence of C4 is dense; here the same
+    shape at a reduced batch and length mixes k = N with keep ratios above and
+    below gamma = 0.8, over ragged lengths. Dense sequences must equal full
+    attention, the others attention over their selection."""
+    w = C4
+    r = K.kvsel_budget(w.block_size, w.n_kvheads, w.head_dim, 2, w.hidden, w.n_blocks, 211e9, 1.7376e15,
+                       keep_floor=w.keep_floor, gamma=w.gamma)
+    assert r.r == 1.0 and r.k == w.n_blocks and r.dense == 1
+    ws = w.scaled(batch=6, seq_len=8192)
+    lens = [8192, 8192, 5000, 8192, 64, 7000]
+    ks = [128, 13, 79, 90, 1, 100]               # N = 128, 128, 79, 128, 1, 110
+    dense_want = [True, False, True, False, True, True]
+    x = generate_layer(ws, 0, device="cuda:0", perm=True, seq_lens=lens)
+    N = x["max_blocks"]
+    page = tuple(x["kv_pages"].shape[1:])
+    host = torch.empty((ws.batch, N) + page, dtype=torch.bfloat16, pin_memory=True)
+    host_tier_layout(x["kv_pages"], x["block_table"], N, out=host)
+    dec = _decoder(ws, x, k_max=N)
+    summ, acc = dec.new_summaries()
+    dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
+    dec.k_per_seq.copy_(torch.tensor(ks, dtype=torch.int32))
+    dec.select(x["q"], summ, x["seq_lens"], gamma=ws.gamma)
+    staging = torch.empty((ws.batch, N) + page, dtype=torch.bfloat16, device="cuda:0")
+    staging.fill_(float("nan"))                  # every attended slot must be written by the fetch
+    from query_aware_sparse_block_gb300 import kvsel as KK
+    dec.attend(x["q"], KK.kv_host(host, N, staging, N), x["seq_lens"])
+    torch.cuda.synchronize()
+    assert K.kvsel_get_error() == 0
+    assert [bool(v) for v in dec.dense_flag.cpu()] == dense_want
+    for b in range(ws.batch):
+        check_sequence(dec, x, b, lens[b], ws.block_size, ks[b], dec.scale, gamma=ws.gamma)
+    # a dense sequence's staging holds all its blocks in order
+    assert torch.equal(staging[2, :79].cpu(), host[2, :79])

@@ -7,8 +7,11 @@ caller workspace.
 Called through the C ABI (ctypes, no torch allocation inside the call) and
 compared with kvsel_score_topk on the same inputs, on two calls in a row:
 indices, spans and flags bit for bit, scores within the tolerance the parity
-tests use. This file is collected last, so a failure here stops a run only
-after every other test has run; it also passes on its own in a fresh process.
+tests use. Without a score output the two-grid form keeps its score rows in
+the static array itself, so those calls are checked too, the second one over
+the first one's leftovers. This file is collected last, so a failure here
+stops a run only after every other test has run; it also passes on its own in
+a fresh process.
 """
 from __future__ import annotations
 
@@ -110,3 +113,52 @@ def test_noalloc_rejects_problems_larger_than_its_scratch(K):
                                     ctypes.c_float(0.0), None, None, None, None, None, None, None, None)
     assert rc == K.KVSEL_ERR_WORKSPACE
     assert b"scratch" in L.kvsel_last_error()
+
+
+@pytest.mark.parametrize("path", ["two_grid", "cluster"])
+def test_noalloc_scores_in_the_static_array_over_two_calls(K, path):
+    """scores_out = NULL: under the two-grid form the score rows live in the
+    static array. Two problems in a row with different lengths and k; the
+    second call runs over the score rows the first one left behind. Every
+    output equals that of the workspace entry point under the same form."""
+    from query_aware_sparse_block_gb300.runtime import SparseDecoder
+    w = C3.scaled(batch=4, seq_len=4096, drift_amp=0.0, layers=1)
+    form = K.KVSEL_SCORE_PATH_TWO_GRID if path == "two_grid" else K.KVSEL_SCORE_PATH_CLUSTER
+    L = K.lib()
+    vp = ctypes.c_void_p
+    runs = [([4096, 33, 4000, 1000], [40, 2, 17, 9]), ([4095, 4096, 0, 640], [3, 40, 5, 20])]
+    prev = K.kvsel_set_score_path(form)
+    try:
+        for lens, ks in runs:
+            x = {k: (v.to("cuda:0") if torch.is_tensor(v) else v)
+                 for k, v in generate_layer(w, 0, seq_lens=lens).items()}
+            dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size,
+                                x["max_blocks"], k_max=40, device="cuda:0")
+            if form == K.KVSEL_SCORE_PATH_CLUSTER:
+                assert K.kvsel_score_path_for(dec.p)[0] == form
+            summ, acc = dec.new_summaries()
+            dec.build_summaries(x["kv_pages"], x["block_table"], x["seq_lens"], summ, acc)
+            dec.k_per_seq.copy_(torch.tensor(ks, dtype=torch.int32))
+            N = [(t + w.block_size - 1) // w.block_size for t in lens]
+            dec.select(x["q"], summ, x["seq_lens"], gamma=0.6, tau_rel=0.5)
+            torch.cuda.synchronize()
+            assert K.kvsel_get_error() == 0
+            none = torch.zeros((w.batch, x["max_blocks"]), device="cuda:0")
+            want = _outputs(dec, none)
+            for t in (dec.sel_idx, dec.n_sel, dec.span_start, dec.span_len, dec.n_spans, dec.dense_flag):
+                t.fill_(-1 if t.dtype != torch.uint8 else 7)
+            torch.cuda.synchronize()
+            stream = vp(torch.cuda.current_stream().cuda_stream)
+            rc = L.kvsel_score_topk_noalloc(ctypes.byref(dec.p), vp(x["q"].data_ptr()), vp(summ.data_ptr()),
+                                            vp(x["seq_lens"].data_ptr()), vp(dec.k_per_seq.data_ptr()),
+                                            ctypes.c_float(0.6), ctypes.c_float(0.5),
+                                            vp(dec.sel_idx.data_ptr()), vp(dec.n_sel.data_ptr()),
+                                            vp(dec.span_start.data_ptr()), vp(dec.span_len.data_ptr()),
+                                            vp(dec.n_spans.data_ptr()), vp(dec.dense_flag.data_ptr()),
+                                            None, stream)
+            assert rc == 0, L.kvsel_last_error()
+            torch.cuda.synchronize()
+            assert K.kvsel_get_error() == 0
+            _same(_outputs(dec, none), want, N)
+    finally:
+        K.kvsel_set_score_path(prev)
