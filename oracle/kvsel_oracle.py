@@ -392,6 +392,13 @@ class BlockCache:
       * Full blocks never change; the block holding the last token changes as
         tokens are appended, so when it is selected its copy is fetched again
         even on a hit (into the slot it already holds).
+      * A prefetch ("KV cache offloading": the Hugging Face Transformers
+        paragraph, the next layer's cache fetched ahead of its use; section
+        "SparDA", the blocks a layer will select fetched on a dedicated stream
+        while the layer before it runs) loads a predicted block list ahead of
+        the selection. It selects nothing: a prefetched block keeps the stamp
+        -1 until a step selects it, so a wrong prediction is evicted before any
+        block that was ever selected.
     """
 
     def __init__(self, slots: int):
@@ -428,3 +435,29 @@ class BlockCache:
             self.last_use[s] = step
             jobs.append((n, s))
         return jobs + refresh, hits
+
+    def prefetch(self, pred, last_block: int):
+        """Load an ascending predicted block list ahead of the step that may
+        select it; returns the fetch jobs (block, slot). The predicted blocks
+        that are resident stay where they are, stamps unchanged. The others,
+        in ascending block order, take the slots that hold no predicted
+        block, smallest (stamp, slot) first, and get the stamp -1. The block
+        holding the last token is not prefetched: appends change it until a
+        step that selects it fetches it."""
+        pred = [int(n) for n in pred]
+        assert len(pred) <= self.slots
+        assert all(a < b for a, b in zip(pred, pred[1:]))
+        keep = {self.slot_of[n] for n in pred if n in self.slot_of}
+        misses = [n for n in pred if n not in self.slot_of and n != last_block]
+        free = [s for s in range(self.slots) if s not in keep]
+        free.sort(key=lambda s: (self.last_use[s], s))
+        jobs = []
+        for n, s in zip(misses, free):
+            old = self.block_in[s]
+            if old >= 0:
+                del self.slot_of[old]
+            self.block_in[s] = n
+            self.slot_of[n] = s
+            self.last_use[s] = -1
+            jobs.append((n, s))
+        return jobs

@@ -520,16 +520,122 @@ def test_c0_step_runs_and_is_self_consistent():
 
 # ------------------------------------------------------------ block cache ---
 
-def test_block_cache_hand_example(golden_dir):
-    c = o.BlockCache(3)
-    for r in _rows(os.path.join(golden_dir, "block_cache_hand_example.txt")):
-        step, sel, last, jobs, hits, blk, use = (p.strip() for p in r.split("|"))
-        got_jobs, got_hits = c.step([int(v) for v in sel.split()], int(step), int(last))
+def _replay_cache_example(cls, path, slots):
+    """Replays a hand-worked cache example (step rows and prefetch rows 'P');
+    returns the first row whose outcome differs, or None."""
+    c = cls(slots)
+    for r in _rows(path):
+        kind, blocks, last, jobs, hits, blk, use = (p.strip() for p in r.split("|"))
+        blocks = [int(v) for v in blocks.split()]
+        if kind == "P":
+            got_jobs, got_hits = c.prefetch(blocks, int(last)), []
+        else:
+            got_jobs, got_hits = c.step(blocks, int(kind), int(last))
         want_jobs = [] if jobs == "-" else [tuple(int(x) for x in j.split(":")) for j in jobs.split()]
-        assert got_jobs == want_jobs, step
-        assert got_hits == ([] if hits == "-" else [int(v) for v in hits.split()])
-        assert c.block_in == [int(v) for v in blk.split()]
-        assert c.last_use == [int(v) for v in use.split()]
+        if (got_jobs != want_jobs or got_hits != ([] if hits == "-" else [int(v) for v in hits.split()])
+                or c.block_in != [int(v) for v in blk.split()] or c.last_use != [int(v) for v in use.split()]):
+            return r
+    return None
+
+
+def test_block_cache_hand_example(golden_dir):
+    assert _replay_cache_example(o.BlockCache, os.path.join(golden_dir, "block_cache_hand_example.txt"), 3) is None
+
+
+def test_block_cache_prefetch_hand_example(golden_dir):
+    path = os.path.join(golden_dir, "block_cache_prefetch_hand_example.txt")
+    assert _replay_cache_example(o.BlockCache, path, 4) is None
+
+
+# Plausible mistakes in the cache, each planted in a copy of the oracle's
+# class; the hand-worked examples must catch every one of them.
+class _MruOrder(o.BlockCache):
+    def step(self, sel, step, last_block):
+        save = list(self.last_use)
+        self.last_use = [-2 - u if u >= 0 else u for u in save]   # newest first among used slots
+        try:
+            jobs, hits = super().step(sel, step, last_block)
+        finally:
+            self.last_use = [step if u == step else (-2 - u if u <= -2 else u) for u in self.last_use]
+        return jobs, hits
+
+
+class _ReversedSlotTies(o.BlockCache):
+    def step(self, sel, step, last_block):
+        self.block_in.reverse(); self.last_use.reverse()
+        self.slot_of = {b: self.slots - 1 - s for b, s in self.slot_of.items()}
+        jobs, hits = super().step(sel, step, last_block)
+        self.block_in.reverse(); self.last_use.reverse()
+        self.slot_of = {b: self.slots - 1 - s for b, s in self.slot_of.items()}
+        return [(n, self.slots - 1 - s) for n, s in jobs], hits
+
+
+class _NoRefresh(o.BlockCache):
+    def step(self, sel, step, last_block):
+        return super().step(sel, step, -1)
+
+
+class _ReversedMissOrder(o.BlockCache):
+    def step(self, sel, step, last_block):
+        jobs, hits = super().step(sel, step, last_block)
+        n_miss = len([j for j in jobs if j[0] not in hits])
+        misses = jobs[:n_miss]
+        blocks = [n for n, _ in misses][::-1]
+        for (n, s), m in zip(misses, blocks):
+            self.block_in[s] = m
+            self.slot_of[m] = s
+        return [(m, s) for (_, s), m in zip(misses, blocks)] + jobs[n_miss:], hits
+
+
+class _PrefetchStamped(o.BlockCache):
+    def prefetch(self, pred, last_block):
+        jobs = super().prefetch(pred, last_block)
+        top = max(self.last_use)
+        for _, s in jobs:
+            self.last_use[s] = top                  # as if selected in the last step
+        return jobs
+
+
+class _PrefetchEvictsPredicted(o.BlockCache):
+    def prefetch(self, pred, last_block):
+        keep = dict(self.slot_of)
+        self.slot_of = {}                           # forget which slots hold predicted blocks
+        misses = [n for n in pred if n not in keep and n != last_block]
+        free = sorted(range(self.slots), key=lambda s: (self.last_use[s], s))
+        self.slot_of = keep
+        jobs = []
+        for n, s in zip(misses, free):
+            old = self.block_in[s]
+            if old >= 0:
+                del self.slot_of[old]
+            self.block_in[s], self.slot_of[n], self.last_use[s] = n, s, -1
+            jobs.append((n, s))
+        return jobs
+
+
+class _PrefetchTakesLastBlock(o.BlockCache):
+    def prefetch(self, pred, last_block):
+        return super().prefetch(pred, -1)
+
+
+class _PrefetchTouchesResident(o.BlockCache):
+    def prefetch(self, pred, last_block):
+        jobs = super().prefetch(pred, last_block)
+        for n in pred:
+            s = self.slot_of.get(n)
+            if s is not None and self.last_use[s] >= 0:
+                self.last_use[s] += 1
+        return jobs
+
+
+@pytest.mark.parametrize("mutant", [_MruOrder, _ReversedSlotTies, _NoRefresh, _ReversedMissOrder,
+                                    _PrefetchStamped, _PrefetchEvictsPredicted,
+                                    _PrefetchTakesLastBlock, _PrefetchTouchesResident])
+def test_block_cache_examples_catch_planted_mistakes(golden_dir, mutant):
+    caught = [_replay_cache_example(mutant, os.path.join(golden_dir, name), slots) is not None
+              for name, slots in (("block_cache_hand_example.txt", 3),
+                                  ("block_cache_prefetch_hand_example.txt", 4))]
+    assert any(caught), mutant.__name__
 
 
 def _random_selections(g, steps, N, k, locality):
@@ -574,6 +680,70 @@ def test_block_cache_invariants_and_lru_order_from_history(seed):
         for b in sel_set:
             last_sel[b] = step
         resident_prev = resident
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_block_cache_prefetch_invariants(seed):
+    g = np.random.default_rng(100 + seed)
+    N, k = 40, int(g.integers(3, 9))
+    slots = 2 * k + int(g.integers(0, 4))
+    c = o.BlockCache(slots)
+    prev = np.array([], dtype=np.int64)
+    for step, sel in enumerate(_random_selections(g, 60, N, k, 0.7)):
+        last = int(g.integers(N - 3, N))
+        # a prediction: most of the previous selection plus a few other blocks
+        extra = g.choice(N, size=int(g.integers(0, k + 1)), replace=False)
+        pred = np.union1d(prev[g.random(len(prev)) < 0.8], extra)[:slots]
+        pred = [int(n) for n in pred]
+        slot_before = dict(c.slot_of)
+        use_before = list(c.last_use)
+        jobs = c.prefetch(pred, last)
+        resident = {b for b in c.block_in if b >= 0}
+        assert all(c.block_in[s] == b for b, s in c.slot_of.items()) and len(c.slot_of) == len(resident)
+        # every predicted block is resident, except a last block that was not
+        assert set(pred) - {last} <= resident
+        if last not in slot_before:
+            assert last not in resident      # never brought in by a prefetch
+        # resident predicted blocks stay where they were, stamps unchanged
+        for n in pred:
+            if n in slot_before:
+                assert c.slot_of[n] == slot_before[n] and c.last_use[slot_before[n]] == use_before[slot_before[n]]
+        # jobs: the other predicted blocks, ascending, stamped -1
+        assert [n for n, _ in jobs] == sorted(n for n in pred if n not in slot_before and n != last)
+        assert all(c.block_in[s] == n and c.last_use[s] == -1 for n, s in jobs)
+        # victims hold no predicted block and come first in (stamp, slot) order
+        evicted = set(slot_before) - resident
+        assert not evicted & set(pred)
+        kept_other = (set(slot_before) & resident) - set(pred)
+        order = lambda b: (use_before[slot_before[b]], slot_before[b])
+        if evicted and kept_other:
+            assert max(map(order, evicted)) < min(map(order, kept_other))
+        # the step then hits every selected block the cache now holds
+        held = dict(c.slot_of)
+        jobs2, hits = c.step(sel, step, last)
+        assert set(hits) == {int(n) for n in sel if int(n) in held}
+        prev = sel
+
+
+def test_block_cache_prefetch_special_cases():
+    # prefetching exactly the next selection leaves that step nothing to fetch
+    # but the block holding the last token
+    c = o.BlockCache(6)
+    c.step([0, 1, 2], 0, 9)
+    assert c.prefetch([1, 4, 5, 9], 9) == [(4, 3), (5, 4)]
+    jobs, hits = c.step([1, 4, 5, 9], 1, 9)
+    assert jobs == [(9, 5)] and hits == [1, 4, 5]
+    # a prediction already resident fetches nothing and changes nothing
+    state = (list(c.block_in), list(c.last_use))
+    assert c.prefetch([1, 4, 9], 9) == [] and (c.block_in, c.last_use) == state
+    assert c.prefetch([], 9) == [] and (c.block_in, c.last_use) == state
+    # a wrong prediction is evicted before any block that was ever selected
+    c = o.BlockCache(4)
+    c.step([0, 1], 0, 50)
+    assert c.prefetch([7], 50) == [(7, 2)]
+    c.step([0, 1], 1, 50)
+    jobs, _ = c.step([2, 3], 2, 50)
+    assert jobs == [(2, 2), (3, 3)] and 7 not in c.slot_of and {0, 1} <= set(c.slot_of)
 
 
 def test_block_cache_special_cases():
