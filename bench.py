@@ -728,14 +728,16 @@ def run_window(wb, stream, steps, plain_ms_per_step, n_sink=1, n_recent=4):
 
 # ------------------------------------------------------------ offload tier ---
 
-def run_offload(device, K, reps=5):
+def run_offload(device, K, reps=5, layer_prefetch=True):
     """C4 shape (64 sequences of 131072 tokens, 32 q / 2 KV heads, d 128, B 64):
     the full K/V in pinned host memory, summaries on the GPU. Reports the
     measured host-to-device copy rate of one large pinned copy, the budget
     model's keep ratio and dense decision for this link, and for the keep
     ratios 5 % (the floor) and 12.5 % the span gather (kvsel_fetch_spans) as
     link bytes per second and as a fraction of the measured copy rate, plus
-    the whole offloaded decode (gather + attention)."""
+    the whole offloaded decode (gather + attention); then the block cache
+    (cross-step reuse) and, with `layer_prefetch`, the layer-ahead prefetch
+    into per-layer caches."""
     import torch
     from query_aware_sparse_block_gb300.runtime import SparseDecoder
     from workloads import C4
@@ -879,10 +881,165 @@ def run_offload(device, K, reps=5):
     torch.cuda.empty_cache()
     res["block_cache"] = run_block_cache(device, K, w, host, page, summ, x, timed, h2d_gbs,
                                          res[f"keep_{w.keep_floor:g}"]["fetch_plus_attend_us"])
+    if layer_prefetch:
+        res["layer_prefetch"] = run_layer_prefetch(device, K, w, host, page, summ, x, h2d_gbs)
     res["copy_unit_sweep"] = run_copy_unit_sweep(device, K, host, timed, h2d_gbs)
     del host
     torch.cuda.empty_cache()
     return res
+
+
+def run_layer_prefetch(device, K, w, host, page, summ, x, h2d_gbs, layers=4, steps=8, rho=0.95,
+                       rounds=3):
+    """Layer-ahead prefetch into per-layer block caches, against the same
+    caches without it, on the C4 shape at the keep floor (k = 102 of 2 048
+    blocks, 64 sequences), for prediction widths m of 2 to 16 blocks. Each
+    of `layers` layers has its own cache (2(k + 16) slots per sequence) and its own drifting queries (q_s = rho q_(s-1) +
+    sqrt(1 - rho^2) e_s); they share the host tier and the summaries. Per
+    step and layer the compute stream selects (keeping the score rows),
+    fetches through the layer's cache and attends. With prefetch, once layer
+    l's fetch is done a second stream takes the next layer's Top-(k + m) of
+    its previous scores (kvsel_select_scores) and prefetches it into that
+    layer's cache (kvsel_cache_prefetch); the next layer's fetch waits for
+    it ("layer_ahead"). The other placement ("step_ahead") predicts on the
+    compute stream right after a layer's select and prefetches that layer's
+    next step on the second stream once its fetch is done, while the
+    following layers run. Steps run back to back behind one bounded device-side delay; the
+    figures are the steady-state time per layer-step (steps 1..), the
+    blocks the compute stream's fetches copied (the critical path) and the
+    blocks prefetched, medians over `rounds` rounds of every variant."""
+    import torch
+    from query_aware_sparse_block_gb300.runtime import BlockPredictor, HostBlockCache, SparseDecoder
+
+    N = w.n_blocks
+    k = w.k_for(w.keep_floor)
+    ms = (2, 4, 8, 16)
+    k_max = k + max(ms)
+    slots = 2 * k_max
+    page_bytes = int(np.prod(page)) * 2
+    seq_lens = x["seq_lens"]
+    decs, caches, preds, scores = [], [], [], []
+    for _ in range(layers):
+        dec = SparseDecoder(w.batch, w.n_qheads, w.n_kvheads, w.head_dim, w.block_size,
+                            x["max_blocks"], k_max=k_max, device=device)
+        dec.k_per_seq.fill_(k)
+        decs.append(dec)
+        caches.append(HostBlockCache(dec, slots, page))
+        preds.append(BlockPredictor(dec, k_max))
+        scores.append([torch.empty((w.batch, x["max_blocks"]), dtype=torch.float32, device=device)
+                       for _ in range(2)])
+    # every query of the run, made before it is timed
+    qs = []
+    for l in range(layers):
+        g = torch.Generator(device=device).manual_seed(900 + l)
+        q = x["q"].float() if l == 0 else torch.randn(x["q"].shape, generator=g, device=device)
+        row = []
+        for s in range(steps):
+            if s:
+                q = rho * q + math.sqrt(1 - rho * rho) * torch.randn(q.shape, generator=g, device=device)
+            row.append(q.to(torch.bfloat16))
+        qs.append(row)
+    compute = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device=device)
+
+    def run(m, mode="layer_ahead"):
+        for c in caches:
+            c.reset()
+        for pr in preds:
+            pr.k_pred.fill_(k + (m or 0))
+        log_fetch = torch.zeros((steps, layers, w.batch), dtype=torch.int32, device=device)
+        log_pref = torch.zeros((steps, layers, w.batch), dtype=torch.int32, device=device)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        pending = [None] * layers
+        last_step = [-1] * layers
+        torch.cuda.synchronize()
+        # a bounded device-side delay (about 10 ms) while the host enqueues the run
+        torch.cuda._sleep(20_000_000)
+        for s in range(steps):
+            ev[s].record(compute)
+            for l in range(layers):
+                dec = decs[l]
+                dec.select(qs[l][s], summ, seq_lens, gamma=w.gamma, scores_out=scores[l][s % 2])
+                if pending[l] is not None:
+                    compute.wait_event(pending[l])
+                    pending[l] = None
+                if m and mode == "step_ahead":
+                    preds[l].from_scores(scores[l][s % 2], seq_lens)
+                caches[l].fetch(host, N, seq_lens, dec.sel_idx, dec.n_sel)
+                log_fetch[s, l].copy_(caches[l].n_fetched)
+                last_step[l] = s
+                fetched = torch.cuda.Event()
+                fetched.record(compute)
+                if m and mode == "step_ahead" and s + 1 < steps:
+                    # this layer's next step, prefetched while the following layers run
+                    copy.wait_event(fetched)
+                    with torch.cuda.stream(copy):
+                        caches[l].prefetch(host, N, seq_lens, preds[l].pred_idx, preds[l].n_pred,
+                                           stream=copy)
+                        log_pref[s + 1, l].copy_(caches[l].n_prefetched)
+                    done = torch.cuda.Event()
+                    done.record(copy)
+                    pending[l] = done
+                dec.attend(qs[l][s], caches[l].kv, seq_lens, use_dense_flag=False)
+                nl = (l + 1) % layers
+                if m and mode == "layer_ahead" and last_step[nl] >= 0 and (nl > l or s + 1 < steps):
+                    copy.wait_event(fetched)
+                    with torch.cuda.stream(copy):
+                        preds[nl].from_scores(scores[nl][last_step[nl] % 2], seq_lens, stream=copy)
+                        caches[nl].prefetch(host, N, seq_lens, preds[nl].pred_idx, preds[nl].n_pred,
+                                            stream=copy)
+                        log_pref[s if nl > l else s + 1, nl].copy_(caches[nl].n_prefetched)
+                    done = torch.cuda.Event()
+                    done.record(copy)
+                    pending[nl] = done
+        ev[steps].record(compute)
+        torch.cuda.synchronize()
+        err = K.kvsel_get_error()
+        if err:
+            raise RuntimeError(f"device error {err} in the layer-prefetch measurement")
+        warm = slice(1, steps)
+        crit = log_fetch[warm].sum().item() / ((steps - 1) * layers)
+        pref = log_pref[warm].sum().item() / ((steps - 1) * layers)
+        return {"layer_us": ev[1].elapsed_time(ev[steps]) * 1e3 / ((steps - 1) * layers),
+                "critical_blocks": crit, "prefetched_blocks": pref}
+
+    variants = [(None, None)] + [(m, mode) for mode in ("layer_ahead", "step_ahead") for m in ms]
+    gc_was_on = gc.isenabled()
+    gc.disable()
+    try:
+        runs = {v: [] for v in variants}
+        for _ in range(rounds):
+            for v in variants:
+                runs[v].append(run(*v))
+    finally:
+        if gc_was_on:
+            gc.enable()
+    out = {"layers": layers, "steps": steps, "rho": rho, "k": k, "slots": slots, "rounds": rounds,
+           "predictor": "Top-(k + m) of the layer's previous-step scores",
+           "layer_ahead": "prediction and prefetch of layer l+1 on the copy stream once layer l's fetch is done",
+           "step_ahead": ("prediction on the compute stream after the layer's select; the prefetch of its "
+                          "next step on the copy stream once its fetch is done")}
+    base = None
+    for v in variants:
+        med = {key: statistics.median(r[key] for r in runs[v]) for key in runs[v][0]}
+        row = {"layer_us": med["layer_us"],
+               "layer_us_per_round": [round(r["layer_us"], 1) for r in runs[v]],
+               "critical_link_bytes_per_layer_step": med["critical_blocks"] * page_bytes,
+               "prefetch_link_bytes_per_layer_step": med["prefetched_blocks"] * page_bytes}
+        if v[0] is None:
+            base = row
+            # the share of the layer-step in which the compute stream's fetch leaves the link idle
+            row["link_idle_fraction"] = 1.0 - (row["critical_link_bytes_per_layer_step"]
+                                               / (h2d_gbs * 1e9 * row["layer_us"] * 1e-6))
+            out["without_prefetch"] = row
+        else:
+            row["speedup_vs_without"] = base["layer_us"] / row["layer_us"]
+            row["critical_bytes_vs_without"] = (row["critical_link_bytes_per_layer_step"]
+                                                / max(1.0, base["critical_link_bytes_per_layer_step"]))
+            out[f"{v[1]}_m_{v[0]}"] = row
+    del caches, decs
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_copy_unit_sweep(device, K, host, timed, h2d_gbs, reps=5):

@@ -302,6 +302,24 @@ KVSEL_API int kvsel_merge_spans(const kvsel_problem* p, const int32_t* sel_idx, 
                       kvsel_stream_t stream);
 
 /*
+ * kvsel_select_scores -- the Top-k, span merge and dense flag of
+ * kvsel_score_topk on score rows the caller already holds ("SparPR KV cache
+ * recovery on a consumer GPU", paragraphs "Query-Aware key-block selection"
+ * and "On-demand local recomputation with cost-aware fallback"), for example
+ * the scores_out of an earlier kvsel_score_topk call: one CTA per sequence
+ * on `stream`. Every output, rule and tie break is that of kvsel_score_topk
+ * on the same scores; k_per_seq may differ from the k the scores were
+ * selected with (a larger k gives a wider list, e.g. a prefetch prediction).
+ * scores: device [batch][max_blocks] fp32 (entries from N_b on are not read).
+ * No workspace. Errors as kvsel_score_topk.
+ */
+KVSEL_API int kvsel_select_scores(const kvsel_problem* p, const float* scores, const int32_t* seq_lens,
+                                  const int32_t* k_per_seq, float gamma, float tau_rel,
+                                  int32_t* sel_idx, int32_t* n_sel, int32_t* span_start,
+                                  int32_t* span_len, int32_t* n_spans, uint8_t* dense_flag,
+                                  kvsel_stream_t stream);
+
+/*
  * kvsel_score_topk_noalloc -- kvsel_score_topk without a caller workspace.
  * The pages describe no such entry point; it exists for callers that cannot
  * allocate device memory: code embedded in a host framework that owns the
@@ -457,6 +475,38 @@ KVSEL_API int kvsel_cache_fetch(const kvsel_problem* p, const kvsel_block_cache*
                                 const int32_t* n_sel, int32_t step, int32_t* n_fetched,
                                 int32_t fetch_ctas, void* ws, size_t ws_bytes,
                                 kvsel_stream_t stream);
+
+/*
+ * kvsel_cache_prefetch -- loads a predicted block list into the cache ahead
+ * of the selection that may ask for it ("KV cache offloading": the Hugging
+ * Face Transformers paragraph, the next layer's cache fetched while the
+ * current one is computed; section "SparDA", the blocks the next layer will
+ * select fetched from pinned host memory on a dedicated stream while the
+ * layer before it runs). The kernels of kvsel_cache_fetch, on `stream`, with
+ * pred_idx / n_pred in place of the selection and three differences:
+ *  - a predicted block that is resident stays in its slot, stamp unchanged;
+ *  - the other predicted blocks, ascending, take the slots that hold no
+ *    predicted block, smallest (last_use, slot) first, and get last_use -1
+ *    (never selected): a wrong prediction is evicted before any block that
+ *    a step selected;
+ *  - the block holding the last token (N_b - 1) is not prefetched (appends
+ *    change it; a selection of it fetches it).
+ * n_fetched[b] (nullable) receives the number of blocks copied. The copy
+ * kernel's CTAs have half the threads of a fetch's and default to one per SM
+ * (fetch_ctas = 0), so that a prefetch on another stream leaves room on each
+ * SM for the score and decode kernels. A later
+ * kvsel_cache_fetch on the same cache must be ordered after this call (same
+ * stream, or an event): both update the cache state and share `ws` if the
+ * caller passes the same one. Calls on different caches may overlap.
+ * pred_idx: device [batch][k_max] int32, strictly ascending per sequence,
+ * n_pred[b] <= k_max entries. Other arguments and errors as
+ * kvsel_cache_fetch (no step).
+ */
+KVSEL_API int kvsel_cache_prefetch(const kvsel_problem* p, const kvsel_block_cache* cache,
+                                   const kvsel_bf16* host_kv, int32_t host_blocks,
+                                   const int32_t* seq_lens, const int32_t* pred_idx,
+                                   const int32_t* n_pred, int32_t* n_fetched, int32_t fetch_ctas,
+                                   void* ws, size_t ws_bytes, kvsel_stream_t stream);
 
 /* Budget inputs ("SparPR KV cache recovery on a consumer GPU", paragraph
  * "Dynamic budget control"). */

@@ -519,39 +519,102 @@ int kvsel_cache_reset(const kvsel_problem* p, const kvsel_block_cache* c, kvsel_
   return cuda_status(e, "cache_reset");
 }
 
+// kvsel_cache_fetch and kvsel_cache_prefetch: the same checks and kernels,
+// on a selection (stamped with `step`) or on a prediction.
+static int cache_fetch_impl(const char* who, const kvsel_problem* p, const kvsel_block_cache* c,
+                            const kvsel_bf16* host_kv, int32_t host_blocks, const int32_t* seq_lens,
+                            const int32_t* idx, const int32_t* n_idx, int32_t step, bool prefetch,
+                            int32_t* n_fetched, int32_t fetch_ctas, void* ws, size_t ws_bytes,
+                            kvsel_stream_t stream) {
+  char msg[160];
+  int r = check_problem(p);
+  if (r) return r;
+  r = check_cache(who, p, c);
+  if (r) return r;
+  if (p->batch == 0) return KVSEL_OK;
+  if (!host_kv || host_blocks <= 0 || !seq_lens || !idx || !n_idx) {
+    std::snprintf(msg, sizeof msg, "%s: host_kv, host_blocks, seq_lens and the block list required", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (step < 0) {
+    std::snprintf(msg, sizeof msg, "%s: step must be >= 0", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (!aligned16(host_kv) || !aligned4(seq_lens) || !aligned4(idx) || !aligned4(n_idx) ||
+      (n_fetched && !aligned4(n_fetched))) {
+    std::snprintf(msg, sizeof msg, "%s: misaligned pointer", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (!ws || ws_bytes < cache_fetch_ws_bytes(*p) || !aligned16(ws)) {
+    std::snprintf(msg, sizeof msg, "%s: workspace missing, small or misaligned", who);
+    return fail(KVSEL_ERR_WORKSPACE, msg);
+  }
+  if (cache_update_smem_bytes(*p, c->slots) > size_t(max_smem_optin())) {
+    std::snprintf(msg, sizeof msg, "%s: slots and k_max exceed shared memory", who);
+    return fail(KVSEL_ERR_UNSUPPORTED, msg);
+  }
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host_kv) != cudaSuccess) {
+    cudaGetLastError();
+    std::snprintf(msg, sizeof msg, "%s: host_kv is not known to CUDA (pin it)", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) {
+    std::snprintf(msg, sizeof msg, "%s: host_kv is not device-mapped pinned memory", who);
+    return fail(KVSEL_ERR_INVALID_ARG, msg);
+  }
+  int* ew = device_error_word();
+  if (!ew) {
+    std::snprintf(msg, sizeof msg, "%s: no CUDA device", who);
+    return fail(KVSEL_ERR_CUDA, msg);
+  }
+  std::snprintf(msg, sizeof msg, "%s launch", who);
+  return cuda_status(launch_cache_fetch(*p, *c, static_cast<const kvsel_bf16*>(at.devicePointer),
+                                        host_blocks, seq_lens, idx, n_idx, step, prefetch, n_fetched,
+                                        ws, fetch_ctas, ew, reinterpret_cast<cudaStream_t>(stream)),
+                     msg);
+}
+
 int kvsel_cache_fetch(const kvsel_problem* p, const kvsel_block_cache* c, const kvsel_bf16* host_kv,
                       int32_t host_blocks, const int32_t* seq_lens, const int32_t* sel_idx,
                       const int32_t* n_sel, int32_t step, int32_t* n_fetched, int32_t fetch_ctas,
                       void* ws, size_t ws_bytes, kvsel_stream_t stream) {
   CallRange range("kvsel_cache_fetch");
+  return cache_fetch_impl("cache_fetch", p, c, host_kv, host_blocks, seq_lens, sel_idx, n_sel, step,
+                          false, n_fetched, fetch_ctas, ws, ws_bytes, stream);
+}
+
+int kvsel_cache_prefetch(const kvsel_problem* p, const kvsel_block_cache* c,
+                         const kvsel_bf16* host_kv, int32_t host_blocks, const int32_t* seq_lens,
+                         const int32_t* pred_idx, const int32_t* n_pred, int32_t* n_fetched,
+                         int32_t fetch_ctas, void* ws, size_t ws_bytes, kvsel_stream_t stream) {
+  CallRange range("kvsel_cache_prefetch");
+  return cache_fetch_impl("cache_prefetch", p, c, host_kv, host_blocks, seq_lens, pred_idx, n_pred,
+                          0, true, n_fetched, fetch_ctas, ws, ws_bytes, stream);
+}
+
+int kvsel_select_scores(const kvsel_problem* p, const float* scores, const int32_t* seq_lens,
+                        const int32_t* k_per_seq, float gamma, float tau_rel, int32_t* sel_idx,
+                        int32_t* n_sel, int32_t* span_start, int32_t* span_len, int32_t* n_spans,
+                        uint8_t* dense_flag, kvsel_stream_t stream) {
+  CallRange range("kvsel_select_scores");
   int r = check_problem(p);
   if (r) return r;
-  r = check_cache("cache_fetch", p, c);
-  if (r) return r;
   if (p->batch == 0) return KVSEL_OK;
-  if (!host_kv || host_blocks <= 0 || !seq_lens || !sel_idx || !n_sel)
-    return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: host_kv, host_blocks, seq_lens, sel_idx, n_sel required");
-  if (step < 0) return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: step must be >= 0");
-  if (!aligned16(host_kv) || !aligned4(seq_lens) || !aligned4(sel_idx) || !aligned4(n_sel) ||
-      (n_fetched && !aligned4(n_fetched)))
-    return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: misaligned pointer");
-  if (!ws || ws_bytes < cache_fetch_ws_bytes(*p) || !aligned16(ws))
-    return fail(KVSEL_ERR_WORKSPACE, "cache_fetch: workspace missing, small or misaligned");
-  if (cache_update_smem_bytes(*p, c->slots) > size_t(max_smem_optin()))
-    return fail(KVSEL_ERR_UNSUPPORTED, "cache_fetch: slots and k_max exceed shared memory");
-  cudaPointerAttributes at;
-  if (cudaPointerGetAttributes(&at, host_kv) != cudaSuccess) {
-    cudaGetLastError();
-    return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: host_kv is not known to CUDA (pin it)");
-  }
-  if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr)
-    return fail(KVSEL_ERR_INVALID_ARG, "cache_fetch: host_kv is not device-mapped pinned memory");
+  if (!scores || !seq_lens || !k_per_seq || !sel_idx || !n_sel || !span_start || !span_len ||
+      !n_spans)
+    return fail(KVSEL_ERR_INVALID_ARG, "select_scores: NULL pointer");
+  if (!aligned4(scores) || !aligned4(seq_lens) || !aligned4(k_per_seq) || !aligned4(sel_idx) ||
+      !aligned4(n_sel) || !aligned4(span_start) || !aligned4(span_len) || !aligned4(n_spans))
+    return fail(KVSEL_ERR_INVALID_ARG, "select_scores: misaligned pointer");
+  if (!std::isfinite(gamma) || !std::isfinite(tau_rel) || tau_rel < 0)
+    return fail(KVSEL_ERR_INVALID_ARG, "select_scores: gamma and tau_rel must be finite, tau_rel >= 0");
   int* ew = device_error_word();
-  if (!ew) return fail(KVSEL_ERR_CUDA, "cache_fetch: no CUDA device");
-  return cuda_status(launch_cache_fetch(*p, *c, static_cast<const kvsel_bf16*>(at.devicePointer),
-                                        host_blocks, seq_lens, sel_idx, n_sel, step, n_fetched, ws,
-                                        fetch_ctas, ew, reinterpret_cast<cudaStream_t>(stream)),
-                     "cache_fetch launch");
+  if (!ew) return fail(KVSEL_ERR_CUDA, "select_scores: no CUDA device");
+  return cuda_status(launch_select_scores(*p, scores, seq_lens, k_per_seq, gamma, tau_rel, sel_idx,
+                                          n_sel, span_start, span_len, n_spans, dense_flag, ew,
+                                          reinterpret_cast<cudaStream_t>(stream)),
+                     "select_scores launch");
 }
 
 int kvsel_fetch_spans(const kvsel_problem* p, const kvsel_kv_src* kv, const int32_t* seq_lens,

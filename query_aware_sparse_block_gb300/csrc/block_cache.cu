@@ -20,6 +20,15 @@
 //      (read through unified virtual addressing) into its pool page.
 // The decode then reads the pool as a paged cache with page_of as its block
 // table, so only the misses cross the host link.
+//
+// A prefetch ("KV cache offloading": the Hugging Face Transformers paragraph,
+// the next layer's cache fetched ahead of its use; section "SparDA", the
+// blocks a layer will select fetched on a dedicated stream while the layer
+// before it runs) is the same two kernels on a predicted block list, with
+// three differences in step 1: a resident predicted block is left as it is
+// (no stamp); the victims are the slots holding no predicted block; a filled
+// slot gets the stamp -1 (never selected), so that a wrong prediction is the
+// first to go. The block holding the last token is not prefetched.
 #include "kvsel_common.cuh"
 #include "kvsel_internal.h"
 
@@ -42,6 +51,7 @@ struct CacheArgs {
   int32_t* n_jobs;       // [batch]
   int32_t* n_fetched;    // [batch], nullable
   int slots, pow2, max_blocks, k_max, B, host_blocks, step;
+  int prefetch;          // 1: the list is a prediction (see above)
   int* err;
 };
 
@@ -52,6 +62,7 @@ __global__ void __launch_bounds__(kUpdThreads) cache_update_kernel(CacheArgs a) 
   int* blk_s = use_s + a.slots;                                                  // [slots]
   int* miss_s = blk_s + a.slots;                                                 // [k_max]
   int* scan_s = miss_s + a.k_max;                                                // [kUpdWarps + 4]
+  unsigned char* pin_s = reinterpret_cast<unsigned char*>(scan_s + kUpdWarps + 4);  // [slots]
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = a.slots;
   int T = a.seq_lens[b];
@@ -67,6 +78,7 @@ __global__ void __launch_bounds__(kUpdThreads) cache_update_kernel(CacheArgs a) 
   for (int s = tid; s < C; s += kUpdThreads) {
     use_s[s] = a.last_use[int64_t(b) * C + s];
     blk_s[s] = a.block_in[int64_t(b) * C + s];
+    pin_s[s] = 0;
   }
   if (tid == 0) scan_s[kUpdWarps] = -1;          // refresh job: pool page, or -1
   __syncthreads();
@@ -84,11 +96,15 @@ __global__ void __launch_bounds__(kUpdThreads) cache_update_kernel(CacheArgs a) 
     const int pg = page_row[blk];
     const int s = pg - b * C;
     if (pg >= 0 && s >= 0 && s < C && blk_s[s] == blk) {
-      use_s[s] = a.step;
-      if (blk == N - 1) scan_s[kUpdWarps] = pg;  // the open block: fetch its copy again
+      if (a.prefetch) {
+        pin_s[s] = 1;                            // stays; no stamp
+      } else {
+        use_s[s] = a.step;
+        if (blk == N - 1) scan_s[kUpdWarps] = pg;  // the open block: fetch its copy again
+      }
     } else {
       if (pg >= 0) latch_error(a.err, KVSEL_ERR_BOUNDS);   // inconsistent state: refetch
-      ++n_miss;
+      if (!a.prefetch || blk != N - 1) ++n_miss;
     }
   }
   // exclusive scan of the miss counts gives each miss its rank in block order
@@ -112,12 +128,14 @@ __global__ void __launch_bounds__(kUpdThreads) cache_update_kernel(CacheArgs a) 
     if (blk < 0 || blk >= N || blk >= a.host_blocks || (i > 0 && sel[i - 1] >= blk)) continue;
     const int pg = page_row[blk];
     const int s = pg - b * C;
-    if (!(pg >= 0 && s >= 0 && s < C && blk_s[s] == blk)) miss_s[r++] = blk;
+    if (!(pg >= 0 && s >= 0 && s < C && blk_s[s] == blk) && (!a.prefetch || blk != N - 1))
+      miss_s[r++] = blk;
   }
-  // ---- victims: slots not stamped this step, ordered by (last_use, slot) ----
+  // ---- victims: slots not stamped this step (a prefetch: holding no
+  // predicted block), ordered by (last_use, slot) ----
   for (int s = tid; s < a.pow2; s += kUpdThreads) {
     unsigned long long key = ~0ull;
-    if (s < C && use_s[s] != a.step)
+    if (s < C && (a.prefetch ? pin_s[s] == 0 : use_s[s] != a.step))
       key = (static_cast<unsigned long long>(static_cast<uint32_t>(use_s[s] + 1)) << 32) | uint32_t(s);
     key_s[s] = key;
   }
@@ -152,7 +170,7 @@ __global__ void __launch_bounds__(kUpdThreads) cache_update_kernel(CacheArgs a) 
     if (old >= 0 && old < a.max_blocks) page_row[old] = -1;
     page_row[blk] = b * C + s;
     blk_s[s] = blk;
-    use_s[s] = a.step;
+    use_s[s] = a.prefetch ? -1 : a.step;
     jobs[q] = make_int2(blk, b * C + s);
   }
   __syncthreads();
@@ -171,12 +189,13 @@ __global__ void __launch_bounds__(kUpdThreads) cache_update_kernel(CacheArgs a) 
 
 // Copies every job's block (one KV page, `block_vec` 16-byte vectors) from
 // the host tier [b][host_blocks][page] to its pool page. Grid (per_seq,
-// batch): the CTAs of a sequence split its job list.
+// batch): the CTAs of a sequence split its job list. blockDim.x is
+// kCopyThreads, or half of it for a prefetch.
 __global__ void __launch_bounds__(kCopyThreads) cache_copy_kernel(
     const kvsel_bf16* __restrict__ host_kv, kvsel_bf16* __restrict__ pool,
     const int2* __restrict__ jobs, const int32_t* __restrict__ n_jobs, int host_blocks,
     int k_max, int64_t block_vec, int* err) {
-  const int b = blockIdx.y, tid = threadIdx.x;
+  const int b = blockIdx.y, tid = threadIdx.x, nt = blockDim.x;
   const int nj = n_jobs[b];
   const int per = (nj + gridDim.x - 1) / gridDim.x;
   const int j0 = blockIdx.x * per, j1 = min(nj, j0 + per);
@@ -189,14 +208,14 @@ __global__ void __launch_bounds__(kCopyThreads) cache_copy_kernel(
     const uint4* src = reinterpret_cast<const uint4*>(host_kv) + (int64_t(b) * host_blocks + job.x) * block_vec;
     uint4* dst = reinterpret_cast<uint4*>(pool) + int64_t(job.y) * block_vec;
     int64_t v = tid;
-    for (; v + (kUnroll - 1) * kCopyThreads < block_vec; v += kUnroll * kCopyThreads) {
+    for (; v + (kUnroll - 1) * nt < block_vec; v += kUnroll * nt) {
       uint4 r[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) r[u] = ld_sys_v4(src + v + u * kCopyThreads);
+      for (int u = 0; u < kUnroll; ++u) r[u] = ld_sys_v4(src + v + u * nt);
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) stg_stream(dst + v + u * kCopyThreads, r[u]);
+      for (int u = 0; u < kUnroll; ++u) stg_stream(dst + v + u * nt, r[u]);
     }
-    for (; v < block_vec; v += kCopyThreads) stg_stream(dst + v, ld_sys_v4(src + v));
+    for (; v < block_vec; v += nt) stg_stream(dst + v, ld_sys_v4(src + v));
   }
 }
 
@@ -210,14 +229,15 @@ size_t cache_fetch_ws_bytes(const kvsel_problem& p) {
 size_t cache_update_smem_bytes(const kvsel_problem& p, int slots) {
   int pow2 = 1;
   while (pow2 < slots) pow2 <<= 1;
-  return size_t(pow2) * 8 + size_t(slots) * 8 + size_t(p.k_max) * 4 + (kUpdWarps + 4) * 4;
+  return size_t(pow2) * 8 + size_t(slots) * 8 + size_t(p.k_max) * 4 + (kUpdWarps + 4) * 4 +
+         size_t(slots);
 }
 
 cudaError_t launch_cache_fetch(const kvsel_problem& p, const kvsel_block_cache& c,
                                const kvsel_bf16* host_kv, int host_blocks,
                                const int32_t* seq_lens, const int32_t* sel_idx,
-                               const int32_t* n_sel, int step, int32_t* n_fetched, void* ws,
-                               int fetch_ctas, int* err, cudaStream_t s) {
+                               const int32_t* n_sel, int step, bool prefetch, int32_t* n_fetched,
+                               void* ws, int fetch_ctas, int* err, cudaStream_t s) {
   if (p.batch == 0) return cudaSuccess;
   CacheArgs a;
   a.seq_lens = seq_lens; a.sel_idx = sel_idx; a.n_sel = n_sel;
@@ -233,6 +253,7 @@ cudaError_t launch_cache_fetch(const kvsel_problem& p, const kvsel_block_cache& 
   a.pow2 = pow2;
   a.max_blocks = p.max_blocks; a.k_max = p.k_max; a.B = p.block_size;
   a.host_blocks = host_blocks; a.step = step; a.err = err;
+  a.prefetch = prefetch ? 1 : 0;
   const size_t smem = cache_update_smem_bytes(p, c.slots);
   cudaError_t e = ensure_smem(reinterpret_cast<const void*>(cache_update_kernel), int(smem));
   if (e != cudaSuccess) return e;
@@ -241,13 +262,17 @@ cudaError_t launch_cache_fetch(const kvsel_problem& p, const kvsel_block_cache& 
   count_launch();
   if (e != cudaSuccess) return e;
   const int64_t block_vec = int64_t(2) * p.n_kvheads * p.block_size * p.head_dim * 2 / 16;
-  // default: eight CTAs per SM, so that a sequence with many misses spreads them over
-  // many CTAs (64 sequences of 64 KiB blocks: 190-200 GB/s with one CTA per SM,
-  // 201-202 GB/s with four to sixteen per SM)
-  const int64_t ctas = fetch_ctas > 0 ? fetch_ctas : 8 * sm_count();
+  // default for a fetch: eight CTAs per SM, so that a sequence with many misses spreads
+  // them over many CTAs (64 sequences of 64 KiB blocks: 190-200 GB/s with one CTA per
+  // SM, 201-202 GB/s with four to sixteen per SM). A prefetch runs beside the other
+  // stream's kernels: one CTA of half the threads per SM, so that it fits on an SM
+  // beside a CTA of the score or decode kernels (registers: 128 x 40 beside 512 x 112
+  // or 256 x 168 of the 65 536)
+  const int64_t ctas = fetch_ctas > 0 ? fetch_ctas : (prefetch ? 1 : 8) * sm_count();
+  const int threads = prefetch ? kCopyThreads / 2 : kCopyThreads;
   const int per_seq = int(std::min<int64_t>(std::max<int64_t>(1, (ctas + p.batch - 1) / p.batch),
                                             int64_t(p.k_max) + 1));
-  cache_copy_kernel<<<dim3(per_seq, p.batch), kCopyThreads, 0, s>>>(
+  cache_copy_kernel<<<dim3(per_seq, p.batch), threads, 0, s>>>(
       host_kv, c.pool, a.jobs, a.n_jobs, host_blocks, p.k_max, block_vec, err);
   count_launch();
   return cudaGetLastError();

@@ -62,6 +62,11 @@ int score_cluster_size(const kvsel_problem& p, bool app);
 // Process-wide choice between the forms (KVSEL_SCORE_PATH_*).
 void set_score_path(int path);
 int score_path();
+cudaError_t launch_select_scores(const kvsel_problem& p, const float* scores,
+                                 const int32_t* seq_lens, const int32_t* k_per_seq, float gamma,
+                                 float tau_rel, int32_t* sel_idx, int32_t* n_sel,
+                                 int32_t* span_start, int32_t* span_len, int32_t* n_spans,
+                                 uint8_t* dense_flag, int* err, cudaStream_t s);
 cudaError_t launch_merge_spans(const kvsel_problem& p, const int32_t* sel_idx,
                                const int32_t* n_sel, int32_t* span_start, int32_t* span_len,
                                int32_t* n_spans, int* err, cudaStream_t s);
@@ -87,7 +92,7 @@ size_t cache_update_smem_bytes(const kvsel_problem& p, int slots);
 cudaError_t launch_cache_fetch(const kvsel_problem& p, const kvsel_block_cache& c,
                                const kvsel_bf16* host_kv, int host_blocks,
                                const int32_t* seq_lens, const int32_t* sel_idx,
-                               const int32_t* n_sel, int step, int32_t* n_fetched, void* ws,
-                               int fetch_ctas, int* err, cudaStream_t s);
+                               const int32_t* n_sel, int step, bool prefetch, int32_t* n_fetched,
+                               void* ws, int fetch_ctas, int* err, cudaStream_t s);
 
 }  // namespace kvsel

@@ -436,6 +436,25 @@ cudaError_t launch_score_topk(const kvsel_problem& p, const kvsel_bf16* q,
   return e;
 }
 
+cudaError_t launch_select_scores(const kvsel_problem& p, const float* scores,
+                                 const int32_t* seq_lens, const int32_t* k_per_seq, float gamma,
+                                 float tau_rel, int32_t* sel_idx, int32_t* n_sel,
+                                 int32_t* span_start, int32_t* span_len, int32_t* n_spans,
+                                 uint8_t* dense_flag, int* err, cudaStream_t s) {
+  if (p.batch == 0) return cudaSuccess;
+  // the select grid of the two-grid form on the caller's rows (it only reads them)
+  ScoreArgs a = make_score_args(p, nullptr, nullptr, seq_lens, k_per_seq, gamma, tau_rel, sel_idx,
+                                n_sel, span_start, span_len, n_spans, dense_flag,
+                                const_cast<float*>(scores), nullptr, 0, 0, err);
+  const size_t sel_smem = ((size_t(p.max_blocks) + 2) * 4 + size_t(p.max_blocks) + 127) / 128 * 128;
+  cudaError_t e = ensure_smem(reinterpret_cast<const void*>(select_kernel), int(sel_smem));
+  if (e != cudaSuccess) return e;
+  select_kernel<<<p.batch, kThreads, sel_smem, s>>>(a);
+  e = cudaGetLastError();
+  count_launch();
+  return e;
+}
+
 cudaError_t launch_merge_spans(const kvsel_problem& p, const int32_t* sel_idx,
                                const int32_t* n_sel, int32_t* span_start, int32_t* span_len,
                                int32_t* n_spans, int* err, cudaStream_t s) {

@@ -113,6 +113,8 @@ _SIGS = {
     "kvsel_set_score_path": (_I, [_I]),
     "kvsel_score_path_for": (_I, [ctypes.POINTER(kvsel_problem), _I, ctypes.POINTER(ctypes.c_int32)]),
     "kvsel_merge_spans": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, _P, _P, _P]),
+    "kvsel_select_scores": (_I, [ctypes.POINTER(kvsel_problem), _P, _P, _P, ctypes.c_float,
+                                 ctypes.c_float, _P, _P, _P, _P, _P, _P, _P]),
     "kvsel_sparse_decode": (_I, [ctypes.POINTER(kvsel_problem), _P, ctypes.POINTER(kvsel_kv_src), _P,
                                  _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P, _P,
                                  ctypes.c_size_t, _P]),
@@ -122,6 +124,9 @@ _SIGS = {
     "kvsel_cache_fetch": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_block_cache), _P,
                                ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_int32, _P,
                                ctypes.c_size_t, _P]),
+    "kvsel_cache_prefetch": (_I, [ctypes.POINTER(kvsel_problem), ctypes.POINTER(kvsel_block_cache), _P,
+                                  ctypes.c_int32, _P, _P, _P, _P, ctypes.c_int32, _P, ctypes.c_size_t,
+                                  _P]),
     "kvsel_budget": (_I, [ctypes.POINTER(kvsel_budget_in), ctypes.POINTER(kvsel_budget_out)]),
     "kvsel_workspace_size": (ctypes.c_size_t, [ctypes.POINTER(kvsel_problem), _I]),
     "kvsel_kv_bytes_per_token": (ctypes.c_int64, [ctypes.c_int32] * 4),
@@ -395,6 +400,37 @@ def kvsel_cache_fetch(p, cache: kvsel_block_cache, host_kv, host_blocks, seq_len
                                    _ptr(n_fetched), int(fetch_ctas), _ptr(ws),
                                    ws.numel() * ws.element_size(), _stream(stream)),
            "kvsel_cache_fetch")
+
+
+def kvsel_cache_prefetch(p, cache: kvsel_block_cache, host_kv, host_blocks, seq_lens, pred_idx, n_pred,
+                         ws, n_fetched=None, fetch_ctas=0, stream=None):
+    """Load a predicted block list into the block cache ahead of the
+    selection that may ask for it."""
+    if host_kv.is_cuda or not host_kv.is_pinned():
+        raise TypeError("host_kv must be a pinned host tensor")
+    for t, dt, n in ((seq_lens, torch.int32, "seq_lens"), (pred_idx, torch.int32, "pred_idx"),
+                     (n_pred, torch.int32, "n_pred"), (n_fetched, torch.int32, "n_fetched")):
+        _expect(t, dt, n)
+    _check(lib().kvsel_cache_prefetch(ctypes.byref(p), ctypes.byref(cache), _ptr(host_kv),
+                                      int(host_blocks), _ptr(seq_lens), _ptr(pred_idx), _ptr(n_pred),
+                                      _ptr(n_fetched), int(fetch_ctas), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _stream(stream)),
+           "kvsel_cache_prefetch")
+
+
+def kvsel_select_scores(p, scores, seq_lens, k_per_seq, sel_idx, n_sel, span_start, span_len, n_spans,
+                        gamma=2.0, tau_rel=0.0, dense_flag=None, stream=None):
+    for t, dt, n in ((scores, torch.float32, "scores"), (seq_lens, torch.int32, "seq_lens"),
+                     (k_per_seq, torch.int32, "k_per_seq"), (sel_idx, torch.int32, "sel_idx"),
+                     (n_sel, torch.int32, "n_sel"), (span_start, torch.int32, "span_start"),
+                     (span_len, torch.int32, "span_len"), (n_spans, torch.int32, "n_spans"),
+                     (dense_flag, torch.uint8, "dense_flag")):
+        _expect(t, dt, n)
+    _check(lib().kvsel_select_scores(ctypes.byref(p), _ptr(scores), _ptr(seq_lens), _ptr(k_per_seq),
+                                     float(gamma), float(tau_rel), _ptr(sel_idx), _ptr(n_sel),
+                                     _ptr(span_start), _ptr(span_len), _ptr(n_spans), _ptr(dense_flag),
+                                     _stream(stream)),
+           "kvsel_select_scores")
 
 
 def kvsel_merge_spans(p, sel_idx, n_sel, span_start, span_len, n_spans, stream=None):

@@ -211,6 +211,7 @@ class HostBlockCache:
         self.block_in = torch.empty((p.batch, self.slots), **i32)
         self.last_use = torch.empty((p.batch, self.slots), **i32)
         self.n_fetched = torch.zeros((p.batch,), **i32)
+        self.n_prefetched = torch.zeros((p.batch,), **i32)
         self.ws = torch.zeros((K.kvsel_workspace_size(p, K.KVSEL_WS_CACHE_FETCH),), dtype=torch.uint8,
                               device=self.device)
         self.desc = K.block_cache(self.slots, self.pool, self.page_of, self.block_in, self.last_use)
@@ -227,3 +228,37 @@ class HostBlockCache:
                             self.step, self.ws, n_fetched=self.n_fetched, fetch_ctas=fetch_ctas,
                             stream=stream)
         self.step += 1
+
+    def prefetch(self, host_kv, host_blocks, seq_lens, pred_idx, n_pred, fetch_ctas=0, stream=None):
+        """Load a predicted block list (e.g. BlockPredictor.pred_idx) ahead
+        of the next fetch(); order that fetch after this call."""
+        K.kvsel_cache_prefetch(self.p, self.desc, host_kv, host_blocks, seq_lens, pred_idx, n_pred,
+                               self.ws, n_fetched=self.n_prefetched, fetch_ctas=fetch_ctas,
+                               stream=stream)
+
+
+class BlockPredictor:
+    """The blocks a layer is expected to select at its next step, with no
+    trained predictor: the k_pred highest-scoring blocks of its score rows
+    from the current step (kvsel_select_scores on the rows a score call wrote
+    to scores_out). Selections of consecutive steps overlap ("KV cache
+    offloading", section "NOSA"), and the blocks that enter the next
+    selection come mostly from just below this step's k-th score, so a list
+    wider than k covers part of the next step's misses."""
+
+    def __init__(self, dec: SparseDecoder, k_pred):
+        p = dec.p
+        if not 0 < int(k_pred) <= p.k_max:
+            raise ValueError("k_pred must be in [1, k_max]")
+        self.p, self.device = p, dec.device
+        i32 = dict(dtype=torch.int32, device=self.device)
+        self.k_pred = torch.full((p.batch,), int(k_pred), **i32)
+        self.pred_idx = torch.zeros((p.batch, p.k_max), **i32)
+        self.n_pred = torch.zeros((p.batch,), **i32)
+        self.span_start = torch.zeros((p.batch, p.k_max), **i32)
+        self.span_len = torch.zeros((p.batch, p.k_max), **i32)
+        self.n_spans = torch.zeros((p.batch,), **i32)
+
+    def from_scores(self, scores, seq_lens, stream=None):
+        K.kvsel_select_scores(self.p, scores, seq_lens, self.k_pred, self.pred_idx, self.n_pred,
+                              self.span_start, self.span_len, self.n_spans, stream=stream)

@@ -34,7 +34,7 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     for n in ("kvsel_build_summaries", "kvsel_score_topk", "kvsel_append_score_topk",
               "kvsel_score_topk_window", "kvsel_merge_spans", "kvsel_cache_reset", "kvsel_cache_fetch",
-              "kvsel_selftest_wait_timeout",
+              "kvsel_cache_prefetch", "kvsel_select_scores", "kvsel_selftest_wait_timeout",
               "kvsel_sparse_decode", "kvsel_budget", "kvsel_fetch_spans",
               "kvsel_workspace_size", "kvsel_kv_bytes_per_token", "kvsel_get_error",
               "kvsel_version"):
@@ -181,6 +181,36 @@ def test_cache_entry_points_validate_before_touching_the_device(K):
     assert fetch(16, -1, 16, 4096) == K.KVSEL_ERR_INVALID_ARG
     assert b"step" in L.kvsel_last_error()
     assert fetch(16, 0, None, 0) == K.KVSEL_ERR_WORKSPACE
+
+    def prefetch(host, pred, ws, nws):
+        return L.kvsel_cache_prefetch(ctypes.byref(p), ctypes.byref(c), host, 64, 4, pred, 4, None, 0,
+                                      ws, nws, None)
+    assert prefetch(None, 4, 16, 4096) == K.KVSEL_ERR_INVALID_ARG
+    assert b"cache_prefetch" in L.kvsel_last_error()
+    assert prefetch(16, None, 16, 4096) == K.KVSEL_ERR_INVALID_ARG
+    assert prefetch(16, 2, 16, 4096) == K.KVSEL_ERR_INVALID_ARG          # misaligned list
+    assert b"misaligned" in L.kvsel_last_error()
+    assert prefetch(16, 4, None, 0) == K.KVSEL_ERR_WORKSPACE
+    c.slots = 7
+    assert prefetch(16, 4, 16, 4096) == K.KVSEL_ERR_INVALID_ARG and b"slots" in L.kvsel_last_error()
+
+
+def test_select_scores_validates_before_touching_the_device(K):
+    L = K.lib()
+    bad = K.problem(1, 8, 8, 96, 16, 64)
+
+    def call(p, scores=16, gamma=1.0, tau=0.0, k=4):
+        return L.kvsel_select_scores(ctypes.byref(p), scores, 4, k, gamma, tau, 4, 4, 4, 4, 4, None,
+                                     None)
+    assert call(bad) == K.KVSEL_ERR_UNSUPPORTED
+    good = K.problem(1, 8, 8, 64, 16, 64)
+    assert call(good, scores=None) == K.KVSEL_ERR_INVALID_ARG
+    assert call(good, k=None) == K.KVSEL_ERR_INVALID_ARG
+    assert call(good, scores=18) == K.KVSEL_ERR_INVALID_ARG and b"misaligned" in L.kvsel_last_error()
+    assert call(good, gamma=float("nan")) == K.KVSEL_ERR_INVALID_ARG
+    assert call(good, tau=-1.0) == K.KVSEL_ERR_INVALID_ARG
+    assert b"tau_rel" in L.kvsel_last_error()
+    assert call(K.problem(0, 8, 8, 64, 16, 64)) == K.KVSEL_OK        # empty batch: nothing to do
 
 
 def test_header_compiles_as_c_and_the_library_links_from_c(K, tmp_path):
