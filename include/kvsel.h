@@ -394,7 +394,11 @@ typedef struct kvsel_kv_src {
  * "NOSA" and "SparDA": kernels that read host memory directly); a block
  * index >= host_blocks latches BOUNDS and is skipped.
  * out: device fp32 output; out_bf16: optional bf16 copy; lse: device fp32.
- * ws: kvsel_workspace_size(p, KVSEL_WS_SPARSE_DECODE) bytes.
+ * ws: kvsel_workspace_size(p, KVSEL_WS_SPARSE_DECODE) bytes (no initial
+ * contents required). Two kernels: the attention grid and a row merge grid
+ * launched as its programmatic dependent.
+ * Errors: UNSUPPORTED when batch * n_kvheads * max_blocks >= 2^31 (the tile
+ * list is counted in int32).
  */
 KVSEL_API int kvsel_sparse_decode(const kvsel_problem* p, const kvsel_bf16* q, const kvsel_kv_src* kv,
                         const int32_t* seq_lens, const int32_t* sel_idx, const int32_t* n_sel,

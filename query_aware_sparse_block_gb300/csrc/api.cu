@@ -659,6 +659,9 @@ int kvsel_sparse_decode(const kvsel_problem* p, const kvsel_bf16* q, const kvsel
     return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: misaligned pointer");
   if (!std::isfinite(softmax_scale))
     return fail(KVSEL_ERR_INVALID_ARG, "sparse_decode: softmax_scale must be finite");
+  // the tile list is counted in int32 (every block of every sequence, dense, per KV head)
+  if (int64_t(p->batch) * p->n_kvheads * p->max_blocks >= (int64_t(1) << 31))
+    return fail(KVSEL_ERR_UNSUPPORTED, "sparse_decode: batch * n_kvheads * max_blocks must be below 2^31");
   if (!ws || ws_bytes < sparse_decode_ws_bytes(*p) || !aligned16(ws))
     return fail(KVSEL_ERR_WORKSPACE, "sparse_decode: workspace missing, small or misaligned");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
