@@ -14,10 +14,18 @@
 //    faster than pairs of 16 KiB ones on GB300 HBM3e. The tiled layout already
 //    carries the 16-byte chunk swizzle (chunk c of row t at c ^ (t % 8)), so
 //    ldmatrix reads are conflict-free.
-//  * Work list: the flattened (sequence, head group, block) tiles are split
-//    into equal contiguous ranges, one per CTA (one CTA per SM), so the HBM
-//    stream is balanced whatever the per-sequence selection sizes are. At the
-//    end of each (sequence, head group) segment every warp stores its online-
+//  * Work list: the flattened (sequence, head group, block) tiles. When every
+//    (sequence, head group) segment that has tiles has the same number nb of
+//    them (every sequence of the batch at the same length and k), each
+//    segment gets the same number m of CTAs, m = min(grid / segments,
+//    nb / kMinTilesPerCta rounded up), and CTA c takes part c % m of segment
+//    c / m: no CTA's range crosses a segment boundary, so a warp loads one
+//    query and stores one state, and the SMs left over stay free for the
+//    Top-k still running in the previous kernel (64 segments on 152 SMs: 128
+//    CTAs, 2.4 % faster than 152 CTAs with ranges across segments). Other
+//    batches are split into equal contiguous ranges, one per CTA, so that the
+//    HBM stream is balanced whatever the per-sequence selection sizes are. At
+//    the end of each (sequence, head group) segment every warp stores its online-
 //    softmax state (max, sum, unnormalised output) to global memory and moves
 //    on without any synchronisation; a second small kernel, launched as a
 //    programmatic dependent of the first so that it is already resident,
@@ -37,6 +45,7 @@
 //    split into bf16 high and low parts so the product keeps ~16 bits.
 //  * Every wait on a copy is bounded; a wait that runs out latches
 //    KVSEL_ERR_TIMEOUT and the warp stops issuing work.
+#include <climits>
 #include <type_traits>
 
 #include "kvsel_common.cuh"
@@ -171,6 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   int* base_s = done_s + 2 * kMaxStages * kRings;                  // [batch+1]
   int* tlen_s = base_s + a.batch + 1;                              // [batch]
   __shared__ int scan_s[kW];
+  __shared__ int nb_s[2];                 // smallest and largest non-zero tile count per segment
 
   // the merge kernel may be scheduled now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -183,6 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   const int h_local = task / kWPH, slice = task % kWPH;
 
   // ---- per-sequence tile counts and prefix ----
+  if (tid == 0) {
+    nb_s[0] = INT_MAX;
+    nb_s[1] = 0;
+  }
+  __syncthreads();
   int carry = 0;
   for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
     const int b = b0 + tid;
@@ -204,6 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
         nb = max(0, min(nb, min(N, a.k_max)));
       }
       tiles_b = nb * a.n_groups;
+      if (nb > 0) {
+        atomicMin(&nb_s[0], nb);
+        atomicMax(&nb_s[1], nb);
+      }
     }
     int x = tiles_b;
 #pragma unroll
@@ -226,7 +245,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   if (tid == 0) base_s[a.batch] = carry;
   __syncthreads();
   const int64_t total = carry;
-  const int A = int(min(int64_t(gridDim.x), max(int64_t(1), (total + kMinTilesPerCta - 1) / kMinTilesPerCta)));
+  // equal segments: m CTAs each, ranges inside one segment
+  const int nbu = nb_s[0] == nb_s[1] ? nb_s[1] : 0;
+  const int n_seg = nbu > 0 ? int(total / nbu) : 0;
+  const int m = n_seg > 0 && n_seg <= int(gridDim.x)
+                    ? min(int(gridDim.x) / n_seg, (nbu + kMinTilesPerCta - 1) / kMinTilesPerCta)
+                    : 0;
+  const int A = m > 0 ? n_seg * m
+                      : int(min(int64_t(gridDim.x), max(int64_t(1), (total + kMinTilesPerCta - 1) / kMinTilesPerCta)));
   if (blockIdx.x == 0) {
     // the CTAs holding each segment's states, for the merge kernel
     for (int64_t seg = tid; seg < int64_t(a.batch) * a.n_groups; seg += kThreads) {
@@ -235,9 +261,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
       int2 info = make_int2(0, 0);
       if (seg_tiles > 0) {
         const int64_t s_start = base_s[b] + int64_t(hg) * seg_tiles, s_end = s_start + seg_tiles;
-        const int first_c = int(((s_start + 1) * A - 1) / total);
-        const int last_c = int((s_end * A - 1) / total);
-        info = make_int2(first_c, last_c - first_c + 1);
+        if (m > 0) {
+          info = make_int2(int(s_start / nbu) * m, m);
+        } else {
+          const int first_c = int(((s_start + 1) * A - 1) / total);
+          const int last_c = int((s_end * A - 1) / total);
+          info = make_int2(first_c, last_c - first_c + 1);
+        }
       }
       a.seg_info[seg] = info;
     }
@@ -256,8 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   }
   if (total == 0) return;
   if (int(blockIdx.x) >= A) return;
-  const int64_t g0 = total * blockIdx.x / A;
-  const int64_t g1 = total * (blockIdx.x + 1) / A;
+  int64_t g0, g1;
+  if (m > 0) {
+    const int k = int(blockIdx.x) / m, part = int(blockIdx.x) % m;
+    g0 = int64_t(k) * nbu + nbu * part / m;
+    g1 = int64_t(k) * nbu + nbu * (part + 1) / m;
+  } else {
+    g0 = total * blockIdx.x / A;
+    g1 = total * (blockIdx.x + 1) / A;
+  }
   if (g0 >= g1) return;
   const int L = int(g1 - g0);
 
