@@ -207,7 +207,9 @@ __device__ __forceinline__ void rank_candidates(const SelectSmem& sm, int m, int
 // rounded steps are non-decreasing in s (no contraction), so a larger score
 // never lands in a lower bin and equal scores share a bin.
 __device__ __forceinline__ int value_bin(float s, float smin, float scale) {
-  return min(kBins - 1, __float2int_rz(__fmul_rn(__fsub_rn(s, smin), scale)));
+  // every candidate key lies in [smin, smax], so the lower clamp never acts; it
+  // keeps a shared-memory index in range should that ever not hold
+  return max(0, min(kBins - 1, __float2int_rz(__fmul_rn(__fsub_rn(s, smin), scale))));
 }
 
 // Top-k + spans + gamma decision for sequence b (whole CTA of kThreads).
