@@ -191,6 +191,29 @@ def test_empty_and_degenerate_sequences(K):
     check_sequence(dec, x, 2, 1, w.block_size, 4, dec.scale)
 
 
+@pytest.mark.parametrize("name,w,lens,k,gamma", [
+    # equal non-empty segments with empty sequences between them: the decode's
+    # equal-segment split, its CTAs mapped past the empty ones
+    ("equal_with_empty", C3.scaled(batch=7, seq_len=3000, layers=1),
+     [3000, 0, 3000, 3000, 0, 0, 3000], 24, 2.0),
+    # every sequence dense at the same length: equal segments of N tiles
+    ("all_dense_equal", C0.scaled(batch=5, seq_len=700), [700] * 5, 30, 0.5),
+    # equal segments of one block each (fewer tiles than a CTA's minimum)
+    ("equal_one_block", C3.scaled(batch=9, seq_len=640, layers=1), [640] * 9, 1, 2.0),
+], ids=lambda v: v if isinstance(v, str) else "")
+def test_decode_split_of_equal_segments(K, name, w, lens, k, gamma):
+    x = to_dev(generate_layer(w, 0, seq_lens=lens), "cuda:0")
+    dec, *_ = _run(K, w, x, k, gamma=gamma)
+    for b, T in enumerate(lens):
+        if T == 0:
+            assert int(dec.n_sel[b]) == 0
+            assert torch.all(dec.out[b] == 0) and torch.all(torch.isneginf(dec.lse[b]))
+        else:
+            check_sequence(dec, x, b, T, w.block_size, k, dec.scale, gamma=gamma)
+    if name == "all_dense_equal":
+        assert bool(dec.dense_flag.all())
+
+
 def test_bad_block_table_is_latched_not_fatal(K):
     w = C0.scaled(batch=2, seq_len=320)
     x = to_dev(generate_layer(w, 0), "cuda:0")
