@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   int* base_s = done_s + 2 * kMaxStages * kRings;                  // [batch+1]
   int* tlen_s = base_s + a.batch + 1;                              // [batch]
   __shared__ int scan_s[kW];
-  __shared__ int nb_s[2];                 // smallest and largest non-zero tile count per segment
+  __shared__ int nbmin_s[kW], nbmax_s[kW];   // per warp: smallest / largest non-zero tile count per segment
 
   // the merge kernel may be scheduled now; it waits for this grid's completion
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -192,13 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   const bool active = task < NA;
   const int h_local = task / kWPH, slice = task % kWPH;
 
-  // ---- per-sequence tile counts and prefix ----
-  if (tid == 0) {
-    nb_s[0] = INT_MAX;
-    nb_s[1] = 0;
-  }
-  __syncthreads();
+  // ---- per-sequence tile counts and prefix; the range of the non-zero counts ----
   int carry = 0;
+  int nb_lo = INT_MAX, nb_hi = 0;
   for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
     const int b = b0 + tid;
     int tiles_b = 0;
@@ -219,9 +215,14 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
         nb = max(0, min(nb, min(N, a.k_max)));
       }
       tiles_b = nb * a.n_groups;
-      if (nb > 0) {
-        atomicMin(&nb_s[0], nb);
-        atomicMax(&nb_s[1], nb);
+    }
+    {
+      const int nb = tiles_b / a.n_groups;
+      const int wmin = __reduce_min_sync(0xffffffffu, nb > 0 ? nb : INT_MAX);
+      const int wmax = __reduce_max_sync(0xffffffffu, nb);
+      if (lane == 0) {
+        nbmin_s[warp] = wmin;
+        nbmax_s[warp] = wmax;
       }
     }
     int x = tiles_b;
@@ -237,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
     for (int w = 0; w < kW; ++w) {
       if (w < warp) before += scan_s[w];
       tot += scan_s[w];
+      nb_lo = min(nb_lo, nbmin_s[w]);
+      nb_hi = max(nb_hi, nbmax_s[w]);
     }
     if (b < a.batch) base_s[b] = carry + before + x - tiles_b;
     carry += tot;
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_decode_kernel(DecodeArgs a
   __syncthreads();
   const int64_t total = carry;
   // equal segments: m CTAs each, ranges inside one segment
-  const int nbu = nb_s[0] == nb_s[1] ? nb_s[1] : 0;
+  const int nbu = nb_lo == nb_hi ? nb_hi : 0;
   const int n_seg = nbu > 0 ? int(total / nbu) : 0;
   const int m = n_seg > 0 && n_seg <= int(gridDim.x)
                     ? min(int(gridDim.x) / n_seg, (nbu + kMinTilesPerCta - 1) / kMinTilesPerCta)
