@@ -60,16 +60,19 @@ def _rows(rng, nmax):
     ]
 
 
-@pytest.mark.parametrize("max_blocks", [1000, 2048, 16384])
+@pytest.mark.parametrize("max_blocks", [1000, 2048, 4096, 4097, 16384])
 def test_threshold_search_paths_match_oracle(K, max_blocks):
-    """max_blocks 1000 and 2048 run the one-warp Top-k (32 and 64 keys per
-    lane); 16384 runs the CTA-wide one."""
+    """Rows of up to 4096 blocks take the one-launch cluster form (the Top-k
+    in the leader CTA, 4096 being the longest row it holds); 4097 and 16384
+    the two-grid form. Both run the same CTA-wide Top-k core."""
     rng = np.random.default_rng(42 + max_blocks)
     rows = _rows(rng, max_blocks)
     batch, Hkv, d, B = len(rows), 1, 64, 16
     k_max = max_blocks
     dev = torch.device("cuda:0")
     p = K.problem(batch, 1, Hkv, d, B, max_blocks, k_max)
+    form, _ = K.kvsel_score_path_for(p)
+    assert form == (K.KVSEL_SCORE_PATH_CLUSTER if max_blocks <= 4096 else K.KVSEL_SCORE_PATH_TWO_GRID)
     summ = torch.zeros((batch, max_blocks, Hkv, d), dtype=torch.bfloat16)
     want_vals = []
     for b, (v, _) in enumerate(rows):
@@ -91,7 +94,7 @@ def test_threshold_search_paths_match_oracle(K, max_blocks):
     scores = torch.zeros((batch, max_blocks), dtype=torch.float32, device=dev)
     ws = torch.zeros(K.kvsel_workspace_size(p, K.KVSEL_WS_SCORE_TOPK), dtype=torch.uint8, device=dev)
     gamma, tau = 0.6, 0.5
-    for _ in range(2):                        # twice: the tickets must come back to zero
+    for _ in range(2):                        # twice: a call leaves nothing behind that changes the next
         K.kvsel_score_topk(p, q.to(dev), summ.to(dev), lens.to(dev), ks.to(dev), sel, n_sel, st, ln, n_sp, ws,
                            gamma=gamma, tau_rel=tau, dense_flag=dense, scores_out=scores)
         torch.cuda.synchronize()
