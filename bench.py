@@ -356,8 +356,9 @@ def run_gpu(args):
         # enqueued on the main stream so far and records when that completes.
         # A layer's score + Top-k call (summary append folded in) runs from the
         # end of the previous layer's merge grid (or the step's start) to the
-        # end of its Top-k grid; its decode call from there to the end of its
-        # merge grid.
+        # end of its last kernel (the cluster launch, or the Top-k grid of the
+        # two-grid form); its decode call from there to the end of its merge
+        # grid.
         cudart = load_cudart()
         side = torch.cuda.Stream(device=device)
         ssp = side.cuda_stream
@@ -542,8 +543,8 @@ def run_gpu(args):
                   "during capture, chained by programmatic dependent launch); per-call durations "
                   "from external event nodes on a side branch of the graph: score_topk (the "
                   "token's summary append folded in) from the end of the previous layer's merge "
-                  "grid to the end of its Top-k grid, sparse_decode from there to the end of its "
-                  "merge grid",
+                  "grid to the end of its last kernel (the cluster launch, or the Top-k grid of the "
+                  "two-grid form), sparse_decode from there to the end of its merge grid",
         "clocks": clk,
         "e2e": e2e,
         "window": window,
