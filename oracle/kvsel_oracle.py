@@ -17,7 +17,11 @@ Sources (page title, section):
   [DKV]     "DKV: Anchor + Low-Rank Differential KV-Cache Compression",
             abstract (flash-style log-sum-exp merge of partial attentions).
   [Offload] "KV cache offloading" wiki article, section "Why the cache leaves
-            the GPU" (KV bytes per token and the transfer-time arithmetic).
+            the GPU" (KV bytes per token and the transfer-time arithmetic),
+            section "NOSA" (blocks kept on the GPU and reused across decode
+            steps under an eviction policy: ``BlockCache.step``), the Hugging
+            Face Transformers paragraph and section "SparDA" (the next layer's
+            blocks fetched ahead of its selection: ``BlockCache.prefetch``).
 
 Every floating-point step is fp64 numpy. Inputs are the bf16 bit patterns
 (uint16 arrays) the GPU receives; they are widened to fp64 exactly here.
